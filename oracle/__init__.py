@@ -1,0 +1,165 @@
+"""f64 CPU oracle for causal prefill attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline / reference
+legs of ``bench.py`` may import this package.  The product path (the CUDA
+library and its Python binding) never imports, links or calls it, and this
+package imports nothing from the product package.
+
+The arithmetic lives in ``fa_oracle.c`` (plain C, IEEE double, libm ``exp``,
+compiled with ``-O2`` and no fast-math).  It computes the plain definition
+
+    O = softmax(scale * Q K^T + causal mask) V
+
+row by row over the full score row, with the bottom-right causal alignment
+(query row i of Sq sees key j iff j <= (Skv - Sq) + i), the contiguous GQA
+grouping hk = hq // (Hq // Hkv), and O = 0 for a row that sees no key.  The
+passages each step follows are cited in the C file's header:
+minfer "28 · r23 — f16-path whole-graph wall decomposition + FA_TKV occupancy
+raise", section 3.2 (the mask), and minfer "53 · r50 — FA_TKV 32->16 occupancy
+experiment", sections 2 and 3.2 (the online softmax it stands in for, the
+fully-masked-row guard, the KV-head index).
+
+Pins (closed forms, invariants, brute force, a library cross-check) are in
+``tests/test_oracle_pins.py``; none of them calls this package to produce an
+expected value.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fa_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``fa_oracle.c`` into ``liboracle.so`` beside it (gcc, -O2, no fast-math)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+           "-fno-fast-math", "-ffp-contract=off", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            d = ctypes.POINTER(ctypes.c_double)
+            i32 = ctypes.c_int
+            lib.oracle_attention.argtypes = [d, d, d, d] + [i32] * 7 + [ctypes.c_double, i32]
+            lib.oracle_attention.restype = i32
+            lib.oracle_attention_rows.argtypes = ([d, d, d] + [i32] * 7 + [ctypes.c_double]
+                                                  + [ctypes.POINTER(ctypes.c_int32),
+                                                     ctypes.c_longlong, d, i32])
+            lib.oracle_attention_rows.restype = i32
+            lib.oracle_probs_row.argtypes = [d, d] + [i32] * 7 + [ctypes.c_double] + [i32] * 3 + [d]
+            lib.oracle_probs_row.restype = i32
+            lib.oracle_plant_mistake.argtypes = [i32]
+            lib.oracle_plant_mistake.restype = i32
+            _lib = lib
+    return _lib
+
+
+# Deliberately wrong variants of the oracle, switched on only by the pin tests
+# to show that the pins reject them (0 is the correct oracle).
+PLANTED_MISTAKES = {
+    "none": 0, "no_scale": 1, "top_left": 2, "mask_off_by_one": 3, "gqa_modulo": 4,
+    "no_normalise": 5, "v_reversed": 6, "no_max_subtract": 7, "exp2": 8, "masked_row_nan": 9,
+}
+
+
+def plant_mistake(kind: str) -> None:
+    """Switch the oracle to one planted mistake (``"none"`` restores it). Tests only."""
+    rc = _load().oracle_plant_mistake(PLANTED_MISTAKES[kind])
+    if rc != 0:
+        raise ValueError(kind)
+
+
+def _f64(x) -> np.ndarray:
+    """Exact upcast of a torch tensor or array-like to contiguous float64."""
+    if hasattr(x, "detach"):  # torch tensor: f16/bf16 -> f64 is exact
+        x = x.detach().to("cpu").double().contiguous().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def default_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover
+        return max(1, os.cpu_count() or 1)
+
+
+def _shape(q, k, v):
+    if q.ndim != 4 or k.ndim != 4 or v.ndim != 4:
+        raise ValueError("q, k, v must be [B, S, H, hd]")
+    B, Sq, Hq, hd = q.shape
+    Bk, Skv, Hkv, hdk = k.shape
+    if (Bk, hdk) != (B, hd) or v.shape != k.shape:
+        raise ValueError(f"shape mismatch q{q.shape} k{k.shape} v{v.shape}")
+    return B, Hq, Hkv, Sq, Skv, hd
+
+
+def attention(q, k, v, causal: bool = True, scale: float | None = None,
+              nthreads: int | None = None) -> np.ndarray:
+    """Full f64 output [B, Sq, Hq, hd] of softmax(scale QK^T + mask) V."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Hq, Hkv, Sq, Skv, hd = _shape(q, k, v)
+    if scale is None:
+        scale = 1.0 / np.sqrt(hd)
+    o = np.zeros((B, Sq, Hq, hd), dtype=np.float64)
+    rc = _load().oracle_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, Hq, Hkv, Sq, Skv, hd,
+                                  int(bool(causal)), float(scale),
+                                  int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError(f"oracle_attention failed with status {rc}")
+    return o
+
+
+def attention_rows(q, k, v, rows, causal: bool = True, scale: float | None = None,
+                   nthreads: int | None = None) -> np.ndarray:
+    """Selected output rows. ``rows`` is an int array [n, 3] of (b, hq, i); returns [n, hd]."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Hq, Hkv, Sq, Skv, hd = _shape(q, k, v)
+    if scale is None:
+        scale = 1.0 / np.sqrt(hd)
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 3))
+    out = np.zeros((r.shape[0], hd), dtype=np.float64)
+    rc = _load().oracle_attention_rows(
+        _ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Sq, Skv, hd, int(bool(causal)), float(scale),
+        r.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), r.shape[0], _ptr(out),
+        int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError(f"oracle_attention_rows failed with status {rc}")
+    return out
+
+
+def probs_row(q, k, b: int, hq: int, i: int, causal: bool = True,
+              scale: float | None = None) -> np.ndarray:
+    """The probability row P[b, hq, i, :] over all Skv keys."""
+    q, k = _f64(q), _f64(k)
+    B, Hq, Hkv, Sq, Skv, hd = _shape(q, k, k)
+    if scale is None:
+        scale = 1.0 / np.sqrt(hd)
+    p = np.zeros((Skv,), dtype=np.float64)
+    rc = _load().oracle_probs_row(_ptr(q), _ptr(k), B, Hq, Hkv, Sq, Skv, hd,
+                                  int(bool(causal)), float(scale), b, hq, i, _ptr(p))
+    if rc != 0:
+        raise ValueError(f"oracle_probs_row failed with status {rc}")
+    return p

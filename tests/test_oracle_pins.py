@@ -1,0 +1,382 @@
+"""Pins for the f64 oracle: facts fixed by the mathematics, not by the oracle.
+
+Each test is chosen so that a plausible slip in the oracle -- a dropped scale,
+a top-left instead of bottom-right causal alignment, an off-by-one in the mask,
+a wrong GQA head index, a transposed operand, a missing max subtraction or
+normalisation -- fails at least one of them (``test_planted_mistakes_are_caught``
+checks that claim for a set of deliberately wrong variants).
+
+The mask rule (a key is visible when it is at or before the query's absolute
+position and inside the stored range) follows minfer "28 · r23 — f16-path
+whole-graph wall decomposition + FA_TKV occupancy raise", section 3.2; the
+fully-masked-row guard follows minfer "53 · r50 — FA_TKV 32->16 occupancy
+experiment", section 3.2.
+"""
+import math
+import os
+from decimal import Decimal, getcontext
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+
+def _rand(shape, seed, scale=1.0):
+    g = np.random.default_rng(seed)
+    return g.standard_normal(shape) * scale
+
+
+# --------------------------------------------------------------------------
+# 1. exact brute force on tiny integer inputs (rational scores, 50-digit exp)
+# --------------------------------------------------------------------------
+
+def _brute_force_exact(q, k, v, causal, scale):
+    """O for integer q/k/v with a dyadic scale: rational scores and a
+    50-significant-digit decimal exp, one key at a time."""
+    getcontext().prec = 50
+    B, Sq, Hq, hd = q.shape
+    _, Skv, Hkv, _ = k.shape
+    G = Hq // Hkv
+    out = np.zeros((B, Sq, Hq, hd))
+    for b in range(B):
+        for h in range(Hq):
+            hk = h // G
+            for i in range(Sq):
+                vis = [j for j in range(Skv) if (not causal) or j <= (Skv - Sq) + i]
+                if not vis:
+                    continue
+                s = {j: scale * sum(Fraction(int(q[b, i, h, d])) * int(k[b, j, hk, d])
+                                    for d in range(hd)) for j in vis}
+                m = max(s.values())
+                e = {j: (Decimal((s[j] - m).numerator) / Decimal((s[j] - m).denominator)).exp()
+                     for j in vis}
+                z = sum(e.values())
+                for d in range(hd):
+                    acc = sum(e[j] * int(v[b, j, hk, d]) for j in vis) / z
+                    out[b, i, h, d] = float(acc)
+    return out
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Sq,Skv", [(4, 4), (3, 5), (5, 3)])
+def test_brute_force_exact_tiny(causal, Sq, Skv):
+    g = np.random.default_rng(7 + Sq * 10 + Skv)
+    q = g.integers(-3, 4, size=(1, Sq, 2, 4)).astype(np.float64)
+    k = g.integers(-3, 4, size=(1, Skv, 1, 4)).astype(np.float64)
+    v = g.integers(-3, 4, size=(1, Skv, 1, 4)).astype(np.float64)
+    scale = Fraction(1, 2)
+    want = _brute_force_exact(q, k, v, causal, scale)
+    got = oracle.attention(q, k, v, causal=causal, scale=0.5)
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-13)
+
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def test_brute_force_4x4_mask_pattern():
+    """Sq = Skv = 4, causal: row i averages exactly over keys 0..i when all
+    scores tie (q = 0), so O row i = mean(v[0..i]) -- the lower-triangular
+    pattern of a square causal mask, worked by hand in the golden fixture."""
+    table = np.loadtxt(os.path.join(GOLDEN, "causal_4x4_prefix_mean.txt"), comments="#")
+    want = table[:, 1:]
+    assert list(table[:, 0]) == [0, 1, 2, 3]
+    v = np.arange(16, dtype=np.float64).reshape(1, 4, 1, 4)
+    q = np.zeros((1, 4, 1, 4))
+    k = np.ones((1, 4, 1, 4))
+    got = oracle.attention(q, k, v, causal=True, scale=1.0)[0, :, 0, :]
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-14)
+
+
+# --------------------------------------------------------------------------
+# 2. identical keys: O row i = mean of V over the visible prefix
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("Sq,Skv", [(7, 7), (5, 12), (1, 9)])
+def test_identical_keys_give_prefix_mean(Sq, Skv):
+    B, Hq, Hkv, hd = 2, 4, 2, 8
+    q = _rand((B, Sq, Hq, hd), 1)
+    kvec = _rand((hd,), 2)
+    k = np.broadcast_to(kvec, (B, Skv, Hkv, hd)).copy()
+    v = _rand((B, Skv, Hkv, hd), 3)
+    got = oracle.attention(q, k, v, causal=True, scale=0.7)
+    csum = np.cumsum(v, axis=1)
+    off = Skv - Sq
+    G = Hq // Hkv
+    for i in range(Sq):
+        n = off + i + 1
+        want = csum[:, n - 1] / n  # [B, Hkv, hd]
+        for h in range(Hq):
+            np.testing.assert_allclose(got[:, i, h], want[:, h // G], rtol=0, atol=1e-12)
+    # non-causal: every row is the mean over all keys
+    got_nc = oracle.attention(q, k, v, causal=False, scale=0.7)
+    want_nc = v.mean(axis=1)
+    for h in range(Hq):
+        np.testing.assert_allclose(got_nc[:, :, h], np.broadcast_to(want_nc[:, None, h // G], got_nc[:, :, h].shape),
+                                   rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# 3. one-hot dominant keys: O row i = the V row of its dominant visible key
+# --------------------------------------------------------------------------
+
+def test_one_hot_dominant_key():
+    Sq = Skv = 12
+    hd = 16
+    perm = np.random.default_rng(5).permutation(Skv)  # key j points along e_perm[j]
+    q = np.zeros((1, Sq, 1, hd))
+    k = np.zeros((1, Skv, 1, hd))
+    for i in range(Sq):
+        q[0, i, 0, i] = 40.0
+    for j in range(Skv):
+        k[0, j, 0, perm[j]] = 1.0
+    v = _rand((1, Skv, 1, hd), 6)
+    inv = np.argsort(perm)  # inv[i] = the key whose direction is e_i
+    for causal in (False, True):
+        got = oracle.attention(q, k, v, causal=causal, scale=1.0)[0, :, 0]
+        for i in range(Sq):
+            jstar = inv[i]
+            if (not causal) or jstar <= i:
+                want = v[0, jstar, 0]  # exp(-40) leakage from the other keys
+                np.testing.assert_allclose(got[i], want, rtol=0, atol=1e-14 * Skv + 1e-15)
+            else:
+                # the dominant key is in the future: all visible scores are 0 -> uniform mean
+                np.testing.assert_allclose(got[i], v[0, :i + 1, 0].mean(axis=0), rtol=0, atol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# 4. rows of P sum to one; masked entries are exactly zero
+# --------------------------------------------------------------------------
+
+def test_probability_rows_sum_to_one_and_respect_mask():
+    B, Sq, Skv, Hq, Hkv, hd = 2, 6, 10, 4, 2, 8
+    q = _rand((B, Sq, Hq, hd), 11, 3.0)
+    k = _rand((B, Skv, Hkv, hd), 12, 3.0)
+    off = Skv - Sq
+    for b in range(B):
+        for h in range(Hq):
+            for i in range(Sq):
+                p = oracle.probs_row(q, k, b, h, i, causal=True, scale=0.5)
+                assert abs(p.sum() - 1.0) < 1e-14
+                assert np.all(p >= 0)
+                assert np.all(p[off + i + 1:] == 0.0)
+                assert np.all(p[:off + i + 1] > 0.0)
+
+
+# --------------------------------------------------------------------------
+# 5. one key: O = v_0 ; causal row 0 of a square case: O = v_0
+# --------------------------------------------------------------------------
+
+def test_single_key_returns_that_value():
+    q = _rand((3, 1, 2, 8), 21)
+    k = _rand((3, 1, 1, 8), 22)
+    v = _rand((3, 1, 1, 8), 23)
+    for causal in (False, True):
+        got = oracle.attention(q, k, v, causal=causal, scale=0.3)
+        np.testing.assert_allclose(got, np.repeat(v, 2, axis=2), rtol=0, atol=1e-15)
+    q2 = _rand((1, 9, 1, 8), 24)
+    k2 = _rand((1, 9, 1, 8), 25)
+    v2 = _rand((1, 9, 1, 8), 26)
+    got = oracle.attention(q2, k2, v2, causal=True, scale=0.3)
+    np.testing.assert_allclose(got[0, 0], v2[0, 0], rtol=0, atol=1e-15)
+
+
+# --------------------------------------------------------------------------
+# 6. GQA equals MHA with K/V repeated per group (contiguous groups)
+# --------------------------------------------------------------------------
+
+def test_gqa_equals_repeated_mha():
+    B, Sq, Skv, Hq, Hkv, hd = 2, 5, 9, 8, 2, 8
+    q = _rand((B, Sq, Hq, hd), 31)
+    k = _rand((B, Skv, Hkv, hd), 32)
+    v = _rand((B, Skv, Hkv, hd), 33)
+    G = Hq // Hkv
+    kr = np.repeat(k, G, axis=2)  # head h of the repeat is kv head h // G
+    vr = np.repeat(v, G, axis=2)
+    for causal in (False, True):
+        a = oracle.attention(q, k, v, causal=causal, scale=0.4)
+        b = oracle.attention(q, kr, vr, causal=causal, scale=0.4)
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-15)
+
+
+# --------------------------------------------------------------------------
+# 7. chunked prefill = the matching slice of a full causal prefill
+# --------------------------------------------------------------------------
+
+def test_chunked_equals_slice_of_full():
+    B, S, Hq, Hkv, hd, n_new = 2, 24, 4, 2, 8, 8
+    q_full = _rand((B, S, Hq, hd), 41)
+    k = _rand((B, S, Hkv, hd), 42)
+    v = _rand((B, S, Hkv, hd), 43)
+    full = oracle.attention(q_full, k, v, causal=True, scale=0.35)
+    chunk = oracle.attention(q_full[:, S - n_new:], k, v, causal=True, scale=0.35)
+    np.testing.assert_allclose(chunk, full[:, S - n_new:], rtol=0, atol=1e-15)
+
+
+# --------------------------------------------------------------------------
+# 8. library cross-check: torch SDPA in float64 with an explicit boolean mask
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Sq,Skv", [(7, 13), (13, 13), (1, 5)])
+def test_matches_torch_sdpa_f64(causal, Sq, Skv):
+    B, Hq, Hkv, hd = 2, 4, 2, 16
+    q = _rand((B, Sq, Hq, hd), 51, 2.0)
+    k = _rand((B, Skv, Hkv, hd), 52, 2.0)
+    v = _rand((B, Skv, Hkv, hd), 53)
+    scale = 0.3
+    got = oracle.attention(q, k, v, causal=causal, scale=scale)
+    G = Hq // Hkv
+    tq = torch.from_numpy(q).permute(0, 2, 1, 3)
+    tk = torch.from_numpy(np.repeat(k, G, axis=2)).permute(0, 2, 1, 3)
+    tv = torch.from_numpy(np.repeat(v, G, axis=2)).permute(0, 2, 1, 3)
+    mask = torch.ones(Sq, Skv, dtype=torch.bool)
+    if causal:  # explicit bottom-right mask (is_causal=True would be top-left)
+        i = torch.arange(Sq)[:, None]
+        j = torch.arange(Skv)[None, :]
+        mask = j <= (Skv - Sq) + i
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask, scale=scale)
+    np.testing.assert_allclose(got, ref.permute(0, 2, 1, 3).numpy(), rtol=0, atol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# 9. shift invariance: adding a constant to every score of a row changes nothing
+# --------------------------------------------------------------------------
+
+def test_row_shift_invariance():
+    B, Sq, Skv, Hq, hd = 1, 6, 6, 2, 8
+    q = _rand((B, Sq, Hq, hd), 61)
+    k = _rand((B, Skv, 1, hd), 62)
+    k[..., 0] = 1.0  # a constant coordinate: q[..., 0] shifts every score of its row
+    v = _rand((B, Skv, 1, hd), 63)
+    a = oracle.attention(q, k, v, causal=True, scale=0.5)
+    q2 = q.copy()
+    q2[..., 0] += np.arange(Sq)[None, :, None] * 7.0 + 100.0
+    b = oracle.attention(q2, k, v, causal=True, scale=0.5)
+    np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# 10. rows that see no key (causal, Skv < Sq) are exactly zero, the rest are not
+# --------------------------------------------------------------------------
+
+def test_fully_masked_rows_are_zero():
+    B, Sq, Skv, Hq, hd = 1, 6, 3, 2, 8
+    q = _rand((B, Sq, Hq, hd), 71)
+    k = _rand((B, Skv, 1, hd), 72)
+    v = _rand((B, Skv, 1, hd), 73)
+    got = oracle.attention(q, k, v, causal=True, scale=0.5)
+    off = Skv - Sq  # -3: rows 0..2 see nothing
+    for i in range(Sq):
+        if off + i < 0:
+            assert np.all(got[0, i] == 0.0)
+        else:
+            assert np.any(got[0, i] != 0.0)
+    # row 3 sees exactly key 0
+    np.testing.assert_allclose(got[0, 3, 0], v[0, 0, 0], rtol=0, atol=1e-15)
+
+
+# --------------------------------------------------------------------------
+# 11. the scale multiplies the scores before the softmax
+# --------------------------------------------------------------------------
+
+def test_scale_applies_to_scores():
+    q = _rand((1, 5, 2, 8), 81)
+    k = _rand((1, 5, 1, 8), 82)
+    v = _rand((1, 5, 1, 8), 83)
+    a = oracle.attention(q * 2.0, k, v, causal=True, scale=0.25)
+    b = oracle.attention(q, k, v, causal=True, scale=0.5)
+    np.testing.assert_allclose(a, b, rtol=0, atol=1e-14)
+    c = oracle.attention(q, k, v, causal=True, scale=0.25)
+    assert np.max(np.abs(b - c)) > 1e-3
+
+
+# --------------------------------------------------------------------------
+# 12. large score ranges do not overflow (max subtraction)
+# --------------------------------------------------------------------------
+
+def test_large_scores_are_stable():
+    q = _rand((1, 4, 1, 8), 91, 300.0)
+    k = _rand((1, 4, 1, 8), 92, 300.0)
+    v = _rand((1, 4, 1, 8), 93)
+    got = oracle.attention(q, k, v, causal=True, scale=1.0)
+    assert np.all(np.isfinite(got))
+    # each row is a convex combination of its visible V rows
+    for i in range(4):
+        lo = v[0, :i + 1, 0].min(axis=0) - 1e-12
+        hi = v[0, :i + 1, 0].max(axis=0) + 1e-12
+        assert np.all(got[0, i, 0] >= lo) and np.all(got[0, i, 0] <= hi)
+
+
+# --------------------------------------------------------------------------
+# 13. the row-sampled entry point and the thread count do not change results
+# --------------------------------------------------------------------------
+
+def test_rows_entry_point_and_threads_agree():
+    B, Sq, Skv, Hq, Hkv, hd = 2, 9, 14, 4, 2, 16
+    q = _rand((B, Sq, Hq, hd), 101)
+    k = _rand((B, Skv, Hkv, hd), 102)
+    v = _rand((B, Skv, Hkv, hd), 103)
+    full1 = oracle.attention(q, k, v, causal=True, scale=0.25, nthreads=1)
+    full8 = oracle.attention(q, k, v, causal=True, scale=0.25, nthreads=8)
+    assert np.array_equal(full1, full8)
+    rows = [(b, h, i) for b in range(B) for h in range(Hq) for i in range(Sq)]
+    got = oracle.attention_rows(q, k, v, rows, causal=True, scale=0.25, nthreads=3)
+    want = np.stack([full1[b, i, h] for (b, h, i) in rows])
+    assert np.array_equal(got, want)
+
+
+def test_bad_arguments_are_rejected():
+    q = np.zeros((1, 2, 3, 4))
+    k = np.zeros((1, 2, 2, 4))
+    with pytest.raises(ValueError):
+        oracle.attention(q, k, k)  # Hq % Hkv != 0
+    with pytest.raises(ValueError):
+        oracle.attention_rows(np.zeros((1, 2, 2, 4)), k, k, [(0, 0, 5)])  # row out of range
+
+
+# --------------------------------------------------------------------------
+# planted mistakes: each wrong variant of the oracle fails at least one pin
+# --------------------------------------------------------------------------
+
+def _pin_battery():
+    """Every pin above, at fixed arguments, as a list of (name, callable)."""
+    return [
+        ("brute_force_causal_3x5", lambda: test_brute_force_exact_tiny(True, 3, 5)),
+        ("brute_force_causal_5x3", lambda: test_brute_force_exact_tiny(True, 5, 3)),
+        ("brute_force_full_4x4", lambda: test_brute_force_exact_tiny(False, 4, 4)),
+        ("mask_pattern_4x4", test_brute_force_4x4_mask_pattern),
+        ("identical_keys", lambda: test_identical_keys_give_prefix_mean(5, 12)),
+        ("one_hot", test_one_hot_dominant_key),
+        ("prob_rows", test_probability_rows_sum_to_one_and_respect_mask),
+        ("single_key", test_single_key_returns_that_value),
+        ("gqa", test_gqa_equals_repeated_mha),
+        ("chunked", test_chunked_equals_slice_of_full),
+        ("sdpa", lambda: test_matches_torch_sdpa_f64(True, 7, 13)),
+        ("shift", test_row_shift_invariance),
+        ("masked_rows", test_fully_masked_rows_are_zero),
+        ("scale", test_scale_applies_to_scores),
+        ("large_scores", test_large_scores_are_stable),
+    ]
+
+
+@pytest.mark.parametrize("kind", [k for k in oracle.PLANTED_MISTAKES if k != "none"])
+def test_planted_mistakes_are_caught(kind):
+    """Plant one mistake in the oracle itself, run every pin, and require that
+    at least one pin fails; the correct oracle passes them all."""
+    failed = []
+    try:
+        oracle.plant_mistake(kind)
+        for name, pin in _pin_battery():
+            try:
+                with np.errstate(all="ignore"):
+                    pin()
+            except AssertionError:
+                failed.append(name)
+    finally:
+        oracle.plant_mistake("none")
+    assert failed, f"no pin caught the planted mistake {kind!r}"
+    for name, pin in _pin_battery():  # and the restored oracle passes again
+        pin()
