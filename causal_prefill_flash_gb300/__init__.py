@@ -1,0 +1,14 @@
+"""GB300-native (sm_103a) causal prefill flash attention.
+
+    O = softmax(scale * Q K^T + causal mask) V
+
+The computation runs in one hand-written CUDA kernel (TMA + mbarrier pipeline,
+tcgen05 MMAs with TMEM accumulators, online softmax) behind the C ABI declared
+in ``include/fa_prefill.h``; this package is its Python binding.
+"""
+from ._build import LIB_PATH, build
+from ._lib import (FA_OK, FaError, attention, debug_status, debug_status_clear, fa_prefill,
+                   fa_prefill_bf16, load, smem_bytes, status_string)
+
+__all__ = ["attention", "fa_prefill", "fa_prefill_bf16", "status_string", "smem_bytes",
+           "debug_status", "debug_status_clear", "FaError", "FA_OK", "build", "load", "LIB_PATH"]

@@ -1,0 +1,138 @@
+"""ctypes binding of libfa_prefill.so: argument marshalling only.
+
+Every step of the attention computation runs in the library's CUDA kernel;
+this module only turns tensors into pointers and sizes, passes the current
+CUDA stream, and raises when the library returns an error.  There is no other
+code path: if the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+from ._build import LIB_PATH
+
+_lock = threading.Lock()
+_lib = None
+
+FA_OK = 0
+STATUS_NAMES = {
+    0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_ALIGNMENT",
+    4: "FA_ERR_SMEM", 5: "FA_ERR_LAUNCH", 6: "FA_ERR_DEVICE",
+}
+
+# (name, restype, argtypes) of every symbol include/fa_prefill.h declares
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SIG = {
+    "fa_prefill": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P]),
+    "fa_prefill_bf16": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P]),
+    "fa_status_string": (ctypes.c_char_p, [_I]),
+    "fa_smem_bytes": (ctypes.c_uint, [_I]),
+    "fa_debug_status": (_I, []),
+    "fa_debug_status_clear": (_I, []),
+}
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+def load():
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; g.build()\"`")
+            lib = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in _SIG.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().fa_status_string(int(status)).decode()
+
+
+def smem_bytes(hd: int) -> int:
+    return int(load().fa_smem_bytes(int(hd)))
+
+
+def debug_status() -> int:
+    return int(load().fa_debug_status())
+
+
+def debug_status_clear() -> int:
+    return int(load().fa_debug_status_clear())
+
+
+def _ptr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(getattr(stream, "cuda_stream", stream))
+
+
+def fa_prefill(q, k, v, o, B, Hq, Hkv, Sq, Skv, hd, causal, scale, stream=None) -> int:
+    """f16 entry point: same arguments as the C function (tensors or raw device
+    pointers for q/k/v/o; ``stream`` None = torch's current stream). Returns the status."""
+    return int(load().fa_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(o), int(B), int(Hq), int(Hkv), int(Sq),
+                                 int(Skv), int(hd), int(causal), float(scale), _stream(stream)))
+
+
+def fa_prefill_bf16(q, k, v, o, B, Hq, Hkv, Sq, Skv, hd, causal, scale, stream=None) -> int:
+    """bf16 entry point: same arguments as the C function. Returns the status."""
+    return int(load().fa_prefill_bf16(_ptr(q), _ptr(k), _ptr(v), _ptr(o), int(B), int(Hq), int(Hkv), int(Sq),
+                                      int(Skv), int(hd), int(causal), float(scale), _stream(stream)))
+
+
+def attention(q, k, v, causal: bool = True, scale: float | None = None, out=None, stream=None):
+    """O = softmax(scale Q K^T + causal mask) V for BSHD CUDA tensors.
+
+    q: [B, Sq, Hq, hd], k/v: [B, Skv, Hkv, hd], all float16 or all bfloat16,
+    contiguous, on the current CUDA device.  Returns O with q's shape and dtype
+    (written into ``out`` when given).  Raises FaError on any library error.
+    """
+    import torch
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors")
+    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in (torch.float16, torch.bfloat16):
+        raise ValueError("q, k, v must all be float16 or all bfloat16")
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("q must be [B, Sq, Hq, hd] and k, v [B, Skv, Hkv, hd]")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous (BSHD)")
+    B, Sq, Hq, hd = q.shape
+    Bk, Skv, Hkv, hdk = k.shape
+    if Bk != B or hdk != hd:
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(hd)
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
+        raise ValueError("out must be a contiguous CUDA tensor like q")
+    fn = fa_prefill_bf16 if q.dtype == torch.bfloat16 else fa_prefill
+    st = fn(q, k, v, out, B, Hq, Hkv, Sq, Skv, hd, int(bool(causal)), scale, stream)
+    if st != FA_OK:
+        raise FaError(st, fn.__name__)
+    return out

@@ -1,0 +1,133 @@
+/*
+ * fa_prefill.h -- C ABI of the GB300 (sm_103a) causal prefill flash-attention
+ * library, libfa_prefill.so.
+ *
+ * The operation is the prefill attention forward pass of a llama-style
+ * inference engine:
+ *
+ *     O = softmax(scale * Q K^T + causal mask) V
+ *
+ * over 16-bit Q, K, V with f32 accumulation, computed tile by tile with an
+ * online softmax (running row max m and row sum l, O rescaled when m moves).
+ * The pages this follows describe that kernel as one launcher call per layer
+ * returning an int status (minfer "49 · r46 (FAP1) — FA audit +
+ * occupancy/bank-conflict levers", section 3.2, the launcher), the validity
+ * mask "key column at or before the query position AND inside the stored KV
+ * range" (minfer "28 · r23 — f16-path whole-graph wall decomposition + FA_TKV
+ * occupancy raise", section 3.2), the KV-head index passed per query head and
+ * the online softmax with its -inf guard (minfer "53 · r50 — FA_TKV 32->16
+ * occupancy experiment", sections 2 and 3.2), and the rule that resource
+ * limits must fail loudly rather than fall back silently (minfer "11 · P5 —
+ * prefill gap session: TM=128 big tiles + FA rewrite", section 3.3).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layout ("BSHD", contiguous, hd fastest):
+ *     q, o : [B][Sq][Hq][hd]        k, v : [B][Skv][Hkv][hd]
+ * GQA: query head hq reads KV head hq / (Hq / Hkv); Hq must be a multiple of Hkv.
+ * Causal alignment is bottom-right: the Sq query rows are the LAST Sq positions
+ * of the Skv keys, so query row i sees key j iff j <= (Skv - Sq) + i.  With
+ * Sq == Skv this is the usual lower-triangular mask; with Sq < Skv it is a
+ * chunk of new rows attending to a cached prefix plus themselves.  A row that
+ * sees no key (possible only when causal and Skv < Sq) gets O = 0.
+ * causal == 0 makes every row see all Skv keys.
+ * scale multiplies Q K^T before the mask and the softmax; it must be finite and
+ * > 0 (1/sqrt(hd) is the usual value).
+ *
+ * Supported: hd in {64, 128}; any B, Sq, Skv >= 0 and Hq, Hkv >= 1 whose
+ * tensors fit TMA's 32-bit coordinates.  B == 0 or Sq == 0 is a no-op
+ * returning FA_OK (the pointers may then be NULL: nothing is read or written);
+ * Skv == 0 writes O = 0 (k and v may then be NULL).
+ *
+ * Memory and ownership: q, k, v, o are DEVICE pointers owned by the caller,
+ * 16-byte aligned, on the current CUDA device; o must not overlap q, k or v.
+ * The library allocates no device memory, keeps no per-call state and never
+ * frees caller memory.  It caches, per device, the kernel attributes it has
+ * set and the driver entry point it uses to encode TMA descriptors.
+ *
+ * Asynchrony: each call validates its arguments on the host, encodes the TMA
+ * descriptors, and enqueues ONE kernel on `stream` (a cudaStream_t; NULL means
+ * the legacy default stream).  It returns once the launch is enqueued; the
+ * result is ready when the stream reaches that point.  Errors that happen while
+ * the kernel runs surface at the caller's next synchronisation; a pipeline
+ * watchdog inside the kernel (see fa_debug_status) turns a stalled wait into a
+ * recorded status instead of a hang.
+ *
+ * Errors are returned, never printed and ignored: every entry point returns
+ * FA_OK (0) or one of the fa_status_t codes below, and on any error no kernel
+ * was launched.
+ */
+#ifndef FA_PREFILL_H
+#define FA_PREFILL_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,  /* null pointer (where one is read or written),
+                                negative size, Hq or Hkv < 1,
+                                Hq % Hkv != 0, non-finite or <= 0 scale,
+                                o overlapping q/k/v                        */
+    FA_ERR_UNSUPPORTED = 2,  /* hd not in {64, 128}, or a tensor too large
+                                for TMA's 32-bit coordinates               */
+    FA_ERR_ALIGNMENT = 3,    /* a pointer not 16-byte aligned (TMA rule)  */
+    FA_ERR_SMEM = 4,         /* the kernel's shared-memory request does not
+                                fit the device, or setting it failed        */
+    FA_ERR_LAUNCH = 5,       /* the launch (or TMA descriptor encode) failed */
+    FA_ERR_DEVICE = 6        /* no current device, or not an sm_103 GPU    */
+} fa_status_t;
+
+/*
+ * fa_prefill -- f16 Q/K/V/O (IEEE binary16), f32 accumulation.
+ *   q      [B][Sq][Hq][hd]  f16, device, read-only
+ *   k, v   [B][Skv][Hkv][hd] f16, device, read-only
+ *   o      [B][Sq][Hq][hd]  f16, device, written (every element)
+ *   causal 0 or 1 (any non-zero value means 1)
+ *   scale  softmax scale applied to Q K^T
+ *   stream cudaStream_t to enqueue on (NULL = legacy default stream)
+ * Returns FA_OK or an fa_status_t error (nothing launched on error).
+ */
+int fa_prefill(const void* q, const void* k, const void* v, void* o,
+               int B, int Hq, int Hkv, int Sq, int Skv, int hd,
+               int causal, float scale, void* stream);
+
+/* fa_prefill_bf16 -- identical to fa_prefill with bfloat16 Q/K/V/O. */
+int fa_prefill_bf16(const void* q, const void* k, const void* v, void* o,
+                    int B, int Hq, int Hkv, int Sq, int Skv, int hd,
+                    int causal, float scale, void* stream);
+
+/* A static, human-readable name for a status code (never NULL). */
+const char* fa_status_string(int status);
+
+/*
+ * fa_smem_bytes -- the dynamic shared memory one CTA of the kernel requests
+ * for head dimension hd (64 or 128), computed from the kernel's own tile
+ * layout (Q tile, K/V stage ring, P tile, barriers, alignment slack).  Returns
+ * 0 for an unsupported hd.  Host-only; no device is touched.  Exposed so the
+ * launcher's request can be checked against the layout, the failure class of
+ * minfer "49 · r46 (FAP1)", section 2.5 (a launcher formula that silently
+ * over-requests shared memory).
+ */
+unsigned int fa_smem_bytes(int hd);
+
+/*
+ * fa_debug_status -- the kernel watchdog word of the current device: 0 when
+ * no kernel has reported a problem since the last clear, otherwise a code
+ * (bits 0-7: which wait gave up; bits 8-31: the CTA index, saturated).  A
+ * pipeline wait that does not complete within the watchdog limit records its
+ * code here, makes its CTA skip its remaining work and exit cleanly (no trap),
+ * so the context stays usable.  Synchronises the device.  Returns -1 if the
+ * word cannot be read.
+ */
+int fa_debug_status(void);
+
+/* Reset the watchdog word of the current device to 0 (synchronous). Returns an fa_status_t. */
+int fa_debug_status_clear(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_PREFILL_H */

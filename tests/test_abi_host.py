@@ -1,0 +1,92 @@
+"""The C ABI on the host, no GPU needed: the library builds and loads, exports
+every symbol include/fa_prefill.h declares, and rejects bad arguments before
+touching a device (resource and argument errors fail loudly -- minfer "11 · P5
+— prefill gap session: TM=128 big tiles + FA rewrite", section 3.3)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa_prefill.h")
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import causal_prefill_flash_gb300 as fa
+    fa.build()
+    fa.load()
+    return fa
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("fa_prefill", "fa_prefill_bf16", "fa_status_string", "fa_smem_bytes",
+              "fa_debug_status", "fa_debug_status_clear"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(fa):
+    lib = ctypes.CDLL(fa.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(fa):
+    for code, name in fa._lib.STATUS_NAMES.items():
+        assert fa.status_string(code).startswith(name)
+    assert fa.status_string(99) == "unknown fa_status_t"
+
+
+def test_smem_request_matches_the_tile_layout(fa):
+    """Q tile + 2-stage K ring + 2-stage V ring + P tile + 14 mbarriers + 16 B of
+    flags + 1 KB alignment slack, for hd = 128 and 64; within the 227 KB opt-in limit."""
+    for hd in (64, 128):
+        q = 128 * hd * 2
+        kv = 128 * hd * 2
+        p = 128 * 128 * 2
+        want = q + 2 * kv + 2 * kv + p + 14 * 8 + 16 + 1024
+        assert fa.smem_bytes(hd) == want
+        assert want <= 227 * 1024
+    assert fa.smem_bytes(96) == 0
+
+
+A = 0x10000  # aligned fake device addresses: validation fails before any use
+
+
+@pytest.mark.parametrize("fn", ["fa_prefill", "fa_prefill_bf16"])
+def test_argument_errors_without_a_device(fa, fn):
+    f = getattr(fa, fn)
+    ok = dict(q=A, k=2 * A, v=3 * A, o=4 * A, B=1, Hq=4, Hkv=2, Sq=8, Skv=8, hd=128, causal=1, scale=0.1)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["q"], a["k"], a["v"], a["o"], a["B"], a["Hq"], a["Hkv"], a["Sq"], a["Skv"], a["hd"],
+                 a["causal"], a["scale"], 0)
+
+    assert call(q=0) == 1 and call(o=0) == 1 and call(k=0) == 1 and call(v=0) == 1
+    assert call(Skv=0, k=0, v=0, hd=96) == 2  # shape errors still reported first
+    assert call(B=-1) == 1 and call(Sq=-3) == 1 and call(Skv=-1) == 1
+    assert call(Hq=0) == 1 and call(Hkv=0) == 1 and call(Hkv=3) == 1
+    assert call(scale=float("nan")) == 1 and call(scale=0.0) == 1 and call(scale=-1.0) == 1
+    assert call(hd=96) == 2 and call(hd=256) == 2
+    assert call(q=A + 8) == 3 and call(o=4 * A + 2) == 3
+    assert call(o=A) == 1  # o overlaps q
+    assert call(Sq=2 ** 31 - 100) == 2
+    # nothing to compute: FA_OK without a device, null pointers allowed
+    assert call(B=0) == 0 and call(Sq=0) == 0
+    assert call(B=0, q=0, k=0, v=0, o=0) == 0 and call(Sq=0, q=0, o=0) == 0
+
+
+def test_python_wrapper_rejects_cpu_tensors(fa):
+    import torch
+    q = torch.zeros((1, 4, 2, 128), dtype=torch.float16)
+    with pytest.raises(ValueError):
+        fa.attention(q, q, q)
