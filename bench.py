@@ -38,8 +38,8 @@ DEFAULT_WORKLOAD = "prefill7b_s2048"
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=20)
@@ -97,7 +97,7 @@ def recorded_traffic(workload: str):
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -115,7 +115,13 @@ class ClockSampler:
                 stdout=self.out, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+        time.sleep(0.5)  # let the sampler start before the load does
+        self.window = None
         return self
+
+    def mark(self, t0: float, t1: float):
+        """Host wall-clock window [t0, t1] of the loaded region."""
+        self.window = (t0, t1)
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -129,16 +135,25 @@ class ClockSampler:
     def summary(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        import datetime
         rows = []
         try:
             with open(self.path) as f:
                 for line in f:
                     parts = [x.strip() for x in line.split(",")]
-                    if len(parts) >= 9:
-                        rows.append(parts)
+                    if len(parts) >= 10:
+                        try:
+                            ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                        except ValueError:
+                            ts = None
+                        rows.append([ts] + parts[1:])
             os.remove(self.path)
         except OSError:
             pass
+        if self.window is not None:
+            inside = [r for r in rows if r[0] is not None and self.window[0] <= r[0] <= self.window[1]]
+            if inside:
+                rows = inside
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
 
@@ -147,17 +162,17 @@ class ClockSampler:
                 return float(x)
             except ValueError:
                 return None
-        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
-        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        sm = [num(r[2]) for r in rows if num(r[2]) is not None]
+        mx = [num(r[3]) for r in rows if num(r[3]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = []
         for i, n in enumerate(names):
-            if any(r[5 + i].lower() == "active" for r in rows):
+            if any(r[6 + i].lower() == "active" for r in rows):
                 reasons.append(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None,
                 "reasons": reasons, "samples": len(rows),
-                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+                "power_w_max": max((num(r[4]) or 0.0) for r in rows)}
 
 
 # --------------------------------------------------------- oracle baseline
@@ -270,6 +285,7 @@ def run_ours(args):
 
     peaks, peak_src = load_peaks()
     with ClockSampler(local) as clocks:
+        t_load0 = time.time()
         for i in range(args.warmup):
             step(i)
         torch.cuda.synchronize()
@@ -282,6 +298,7 @@ def run_ours(args):
             step(i)
         e1.record(stream)
         torch.cuda.synchronize()
+        clocks.mark(t_load0, time.time())
         barrier()
         torch.cuda.synchronize()
     ms_total = e0.elapsed_time(e1)

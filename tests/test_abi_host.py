@@ -46,13 +46,15 @@ def test_status_strings(fa):
 
 
 def test_smem_request_matches_the_tile_layout(fa):
-    """Q tile + 2-stage K ring + 2-stage V ring + P tile + 14 mbarriers + 16 B of
-    flags + 1 KB alignment slack, for hd = 128 and 64; within the 227 KB opt-in limit."""
-    for hd in (64, 128):
+    """Two query tiles + a ring of K/V slots (5 at hd = 128, 8 at hd = 64) +
+    one mbarrier for Q, a full/empty pair per slot, two each for S ready, P
+    ready, and one each for the final O and the abort drain + 16 B of flags +
+    1 KB alignment slack; within the 227 KB opt-in limit."""
+    for hd, nslot in ((64, 8), (128, 5)):
         q = 128 * hd * 2
-        kv = 128 * hd * 2
-        p = 128 * 128 * 2
-        want = q + 2 * kv + 2 * kv + p + 14 * 8 + 16 + 1024
+        slot = 128 * hd * 2
+        bars = 1 + 2 * nslot + 2 + 2 + 2
+        want = 2 * q + nslot * slot + bars * 8 + 16 + 1024
         assert fa.smem_bytes(hd) == want
         assert want <= 227 * 1024
     assert fa.smem_bytes(96) == 0
