@@ -59,9 +59,17 @@ namespace fa {
 
 constexpr int BM = 128;           // query rows per tile == TMEM lanes == M of both MMAs
 constexpr int BN = 128;           // keys per KV tile == N of S = Q K^T == K of P V
-constexpr int NUM_THREADS = 320;  // warps 0-7 softmax (two warpgroups), 8 MMA, 9 producer
+constexpr int NUM_THREADS = 384;  // warpgroups 0, 1: softmax of tiles A, B; warpgroup 2: MMA, producer
 constexpr int MMA_WARP = 8;
-constexpr int PRODUCER_WARP = 9;
+constexpr int PRODUCER_WARP = 9;   // warps 10 and 11 only complete warpgroup 2
+// Register budgets: launched at 168 per thread (65536 / 384, rounded down to
+// a multiple of 8); warpgroup 2 gives registers back so the softmax
+// warpgroups can hold a whole S row (128 f32) without spilling.
+constexpr uint32_t LAUNCH_REGS = 168;
+constexpr uint32_t REGS_SOFTMAX = 208;
+constexpr uint32_t REGS_CONTROL = 56;
+static_assert(128 * REGS_CONTROL + 256 * REGS_SOFTMAX <= NUM_THREADS * LAUNCH_REGS,
+              "register split exceeds the launch allocation");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_TAU = 8.0f;  // lazy rescale threshold in log2 units (P <= 2^8)
 constexpr unsigned long long WATCHDOG_NS = 2000000000ull;  // 2 s per wait
@@ -164,7 +172,7 @@ __device__ unsigned int g_fa_status = 0;
 
 // Slow path of a bounded wait: poll, then give up after the watchdog limit
 // (or as soon as another role of this CTA has given up).
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+__device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                        unsigned long long limit_ns, uint32_t code) {
   const uint64_t t0 = ptx::globaltimer_ns();
   while (true) {
@@ -196,7 +204,7 @@ __device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity,
 }
 
 // Drain wait used only on the abort path: bounded, ignores the abort flag.
-__device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
   const uint64_t t0 = ptx::globaltimer_ns();
   while (!ptx::mbar_try_wait(bar, parity)) {
     if (ptx::globaltimer_ns() - t0 > limit_ns) {
@@ -273,6 +281,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = misc[0];
 
+  if (warp >= MMA_WARP) {
+  ptx::setmaxnreg_dec<REGS_CONTROL>();
   if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -335,7 +345,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ptx::mma_f16_ts(d, a + kk * 8, ptx::sdesc_sw128(v + kk * (16 * 128), BN * 128, 1024), IDESC_O,
                           (acc || kk > 0) ? 1u : 0u);
       };
-      const int nx[2] = {nA, nB};
       bool ok = wait_bar(bQ, 0, abort_flag, p.watchdog_ns, WD_MMA_Q);
       if (ok && n > 0) {
         ok = wait_bar(bFull(0), 0, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);
@@ -356,15 +365,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ok = wait_bar(bFull(sk), (ik / NSLOT) & 1, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);
           if (!ok) break;
         }
+#pragma unroll
         for (int x = 0; x < 2; ++x) {
-          if (j < nx[x]) {
+          const int nX = x == 0 ? nA : nB;
+          if (j < nX) {
             ok = wait_bar(bPfull(x), j & 1, abort_flag, p.watchdog_ns, WD_MMA_P_FULL);
             if (!ok) break;
             ptx::tc_fence_after();
             issue_pv(x, sv, j > 0);
           }
           if (x == 1) ptx::mma_commit(bEmpty(sv));  // V_j no longer needed once PV_B(j) is done
-          if (more && j + 1 < nx[x]) issue_s(x, sk);
+          if (more && j + 1 < nX) issue_s(x, sk);
         }
         if (!ok) break;
         if (more) ptx::mma_commit(bEmpty(sk));
@@ -376,14 +387,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         drain_wait(bDrain, 0, p.watchdog_ns);
       }
     }
+  }
   } else {
+    ptx::setmaxnreg_inc<REGS_SOFTMAX>();
     // -------------------------------------------------------------- softmax
     const int x = warp >> 2;          // query tile of this warpgroup
     const int r = threadIdx.x & 127;  // row in the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + L::TM_S + x * BN;
     const uint32_t tO = tmem + lane_off + L::TM_O + x * HD;
-    const int q0 = w.q0[x];
+    const int q0 = x == 0 ? w.q0[0] : w.q0[1];
+    const int hqx = x == 0 ? w.hq[0] : w.hq[1];
+    const bool hasx = x == 0 ? w.has[0] : w.has[1];
     const int nX = x == 0 ? nA : nB;
     const int off = p.Skv - p.Sq;
     const int kv_all = p.causal ? min(p.Skv, off + q0 + 1) : p.Skv;       // keys every row sees
@@ -481,12 +496,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ok = warp_wait_bar(bOfinal, 0, abort_flag, p.watchdog_ns, WD_SOFTMAX_O_DONE);
       if (ok) ptx::tc_fence_after();
     }
-    if (ok && w.has[x]) {
+    if (ok && hasx) {
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
       const int qrow = q0 + r;
       const bool row_ok = qrow < p.Sq;
       uint4* dst =
-          reinterpret_cast<uint4*>(p.o + ((static_cast<size_t>(w.b) * p.Sq + qrow) * p.Hq + w.hq[x]) * HD);
+          reinterpret_cast<uint4*>(p.o + ((static_cast<size_t>(w.b) * p.Sq + qrow) * p.Hq + hqx) * HD);
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c) {
         uint32_t orr[32];

@@ -180,6 +180,18 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
   for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i])::"memory");
 }
 
+// Per-warpgroup register budget changes (all 128 threads of the warpgroup
+// execute them).  .inc blocks until the CTA's pool has the registers, so the
+// budgets of all warpgroups must add up to at most the launch allocation.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------- descriptors
 
 // Shared-memory matrix descriptor for a tile stored in the 128-byte swizzle
