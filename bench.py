@@ -59,6 +59,24 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest `value` over all ranks (identity without a process group).
+    Timing uses it so the whole job is as slow as its slowest rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_step_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job TFLOP/s: every rank runs its own replica of the workload (weak
+    scaling), all ranks' flops over the slowest rank's step time."""
+    return flops_per_step_per_rank * world / (ms_per_step * 1e-3) / 1e12
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -301,14 +319,10 @@ def run_ours(args):
         clocks.mark(t_load0, time.time())
         barrier()
         torch.cuda.synchronize()
-    ms_total = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(e0.elapsed_time(e1), dev)
     ms_step = ms_total / args.steps
     flops = w.flops()
-    value = flops * world / (ms_step * 1e-3) / 1e12
+    value = job_throughput(flops, world, ms_step)
     watchdog = fa.debug_status()
 
     # end to end through the public API: pinned host inputs -> device -> kernel -> host O
@@ -337,12 +351,8 @@ def run_ours(args):
             e2e_step()
         a1.record(stream)
         torch.cuda.synchronize()
-        ms_e2e = a0.elapsed_time(a1) / args.e2e_steps
-        if world > 1:
-            t = torch.tensor([ms_e2e], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ms_e2e = float(t.item())
-        e2e = {"value": flops * world / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+        ms_e2e = max_over_ranks(a0.elapsed_time(a1) / args.e2e_steps, dev)
+        e2e = {"value": job_throughput(flops, world, ms_e2e), "unit": "TFLOP/s",
                "ms_per_step": ms_e2e,
                "h2d_bytes_per_step": int((q.numel() + k.numel() + v.numel()) * q.element_size()),
                "d2h_bytes_per_step": int(q.numel() * q.element_size())}

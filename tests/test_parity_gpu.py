@@ -258,3 +258,35 @@ def test_workload_full_size_sampled_rows(idx):
         G = w.Hq // w.Hkv
         v0 = v[:, 0].double().repeat_interleave(G, dim=1)  # [B, Hq, hd]
         _check(got[:, 0], v0.numpy(), w.dtype, "row 0 = v_0")
+
+
+# ------------------------------------------------------ many-CTA / sparse grids
+
+def _sampled_case(B, Hq, Hkv, Sq, Skv, hd, dtype, seed, causal=True, n_rows=512):
+    w, (q, k, v) = _inputs(B, Hq, Hkv, Sq, Skv, hd, dtype, seed)
+    got = _run_gpu(q, k, v, causal, w.scale)
+    rows = W.sample_rows(w, n_rows, seed=seed)
+    want = oracle.attention_rows(q, k, v, rows.numpy(), causal=causal, scale=w.scale)
+    g = got[rows[:, 0].long(), rows[:, 2].long(), rows[:, 1].long()]
+    _check(g, want, dtype, f"sampled B{B} H{Hq}/{Hkv} Sq{Sq} Skv{Skv} hd{hd}")
+    return got, rows
+
+
+def test_many_units_with_empty_ones_between():
+    """Many more CTAs than SMs, most of them with no visible key (causal,
+    Skv << Sq): CTAs with nothing to stream write zeros, and every row before
+    Sq - Skv must come out exactly 0."""
+    Sq, Skv = 8192, 1000
+    got, _ = _sampled_case(1, 40, 40, Sq, Skv, 128, "f16", 21)
+    assert torch.all(got[:, : Sq - Skv] == 0)
+    assert torch.isfinite(got).all()
+
+
+def test_odd_gqa_group_pairs_row_tiles_over_rounds():
+    """G = 3 (odd): a CTA pairs two row tiles of one head (the second may be
+    past Sq); B = 4 gives several waves of CTAs."""
+    _sampled_case(4, 12, 4, 1000, 1000, 128, "bf16", 22)
+
+
+def test_even_gqa_many_rounds_hd64():
+    _sampled_case(2, 16, 4, 3000, 3000, 64, "f16", 23)
