@@ -29,6 +29,10 @@ _I = ctypes.c_int
 _SIG = {
     "fa_prefill": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P]),
     "fa_prefill_bf16": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P]),
+    "fa_prefill_ws": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, ctypes.c_size_t, _P]),
+    "fa_prefill_ws_bf16": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, ctypes.c_size_t,
+                                _P]),
+    "fa_workspace_bytes": (ctypes.c_size_t, [_I]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_smem_bytes": (ctypes.c_uint, [_I]),
     "fa_debug_status": (_I, []),
@@ -105,12 +109,50 @@ def fa_prefill_bf16(q, k, v, o, B, Hq, Hkv, Sq, Skv, hd, causal, scale, stream=N
                                       int(Skv), int(hd), int(causal), float(scale), _stream(stream)))
 
 
-def attention(q, k, v, causal: bool = True, scale: float | None = None, out=None, stream=None):
+def fa_prefill_ws(q, k, v, o, B, Hq, Hkv, Sq, Skv, hd, causal, scale, workspace, workspace_bytes,
+                  stream=None) -> int:
+    """Stream-K entry point (f16): the C function's arguments. Returns the status."""
+    return int(load().fa_prefill_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(o), int(B), int(Hq), int(Hkv), int(Sq),
+                                    int(Skv), int(hd), int(causal), float(scale), _ptr(workspace),
+                                    int(workspace_bytes), _stream(stream)))
+
+
+def fa_prefill_ws_bf16(q, k, v, o, B, Hq, Hkv, Sq, Skv, hd, causal, scale, workspace, workspace_bytes,
+                       stream=None) -> int:
+    """Stream-K entry point (bf16): the C function's arguments. Returns the status."""
+    return int(load().fa_prefill_ws_bf16(_ptr(q), _ptr(k), _ptr(v), _ptr(o), int(B), int(Hq), int(Hkv),
+                                         int(Sq), int(Skv), int(hd), int(causal), float(scale), _ptr(workspace),
+                                         int(workspace_bytes), _stream(stream)))
+
+
+def workspace_bytes(hd: int) -> int:
+    return int(load().fa_workspace_bytes(int(hd)))
+
+
+_workspaces = {}
+
+
+def workspace_for(device, hd: int, stream=None):
+    """A zero-filled workspace for the stream-K path, one per (device, stream, hd),
+    allocated once by torch and reused (calls on one stream never overlap)."""
+    import torch
+    key = (str(device), int(_stream(stream)) if stream is not None else None, int(hd))
+    ws = _workspaces.get(key)
+    if ws is None:
+        ws = torch.zeros(workspace_bytes(hd), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def attention(q, k, v, causal: bool = True, scale: float | None = None, out=None, stream=None,
+              split: bool = False):
     """O = softmax(scale Q K^T + causal mask) V for BSHD CUDA tensors.
 
     q: [B, Sq, Hq, hd], k/v: [B, Skv, Hkv, hd], all float16 or all bfloat16,
     contiguous, on the current CUDA device.  Returns O with q's shape and dtype
-    (written into ``out`` when given).  Raises FaError on any library error.
+    (written into ``out`` when given).  ``split=True`` uses the load-balanced
+    stream-K kernel with a cached workspace.  Raises FaError on any library
+    error.
     """
     import torch
     if not (q.is_cuda and k.is_cuda and v.is_cuda):
@@ -131,8 +173,13 @@ def attention(q, k, v, causal: bool = True, scale: float | None = None, out=None
         out = torch.empty_like(q)
     elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
         raise ValueError("out must be a contiguous CUDA tensor like q")
-    fn = fa_prefill_bf16 if q.dtype == torch.bfloat16 else fa_prefill
-    st = fn(q, k, v, out, B, Hq, Hkv, Sq, Skv, hd, int(bool(causal)), scale, stream)
+    if split:
+        fn = fa_prefill_ws_bf16 if q.dtype == torch.bfloat16 else fa_prefill_ws
+        ws = workspace_for(q.device, hd, stream)
+        st = fn(q, k, v, out, B, Hq, Hkv, Sq, Skv, hd, int(bool(causal)), scale, ws, ws.numel(), stream)
+    else:
+        fn = fa_prefill_bf16 if q.dtype == torch.bfloat16 else fa_prefill
+        st = fn(q, k, v, out, B, Hq, Hkv, Sq, Skv, hd, int(bool(causal)), scale, stream)
     if st != FA_OK:
         raise FaError(st, fn.__name__)
     return out

@@ -51,6 +51,8 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
+#include <vector>
 
 #include "fa_prefill.h"
 #include "sm103_ptx.cuh"
@@ -83,6 +85,7 @@ enum : uint32_t {
   WD_SOFTMAX_S_FULL = 7,
   WD_SOFTMAX_O_DONE = 8,
   WD_DRAIN = 9,
+  WD_MERGE_FLAG = 12,
 };
 
 // Shared-memory plan of one CTA, all offsets from a 1024-byte aligned base.
@@ -97,8 +100,8 @@ struct Layout {
   static constexpr uint32_t OFF_Q = 0;               // Q_A, Q_B
   static constexpr uint32_t OFF_RING = 2 * Q_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_RING + NSLOT * SLOT_BYTES;
-  // q_full, full[NSLOT], empty[NSLOT], s_full[2], p_full[2], o_final, drain
-  static constexpr uint32_t NUM_BARS = 1 + 2 * NSLOT + 2 + 2 + 2;
+  // q_full, full[NSLOT], empty[NSLOT], s_full[2], p_full[2], o_final, drain, o_staged[2]
+  static constexpr uint32_t NUM_BARS = 1 + 2 * NSLOT + 2 + 2 + 2 + 2;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
   static constexpr uint32_t BYTES = OFF_MISC + 16;
   static constexpr uint32_t REQUEST = BYTES + 1024;  // slack to align the dynamic base
@@ -107,6 +110,7 @@ struct Layout {
   static constexpr uint32_t TM_O = 2 * BN;
   static_assert(TM_O + 2 * HD <= TMEM_COLS, "TMEM plan");
   static_assert(OFF_RING % 1024 == 0 && SLOT_BYTES % 1024 == 0, "swizzle atoms");
+  static_assert(SLOT_BYTES == BM * HD * 2 && NSLOT >= 2, "each O tile is staged in a ring slot");
 };
 
 struct Params {
@@ -228,7 +232,8 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 template <int HD, bool BF16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fa_prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV, const Params p) {
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                      const Params p) {
   using L = Layout<HD>;
   constexpr int NSLOT = L::NSLOT;
   extern __shared__ uint8_t smem_raw[];
@@ -246,6 +251,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto bPfull = [&](int x) { return bar + 8u * (3 + 2 * NSLOT + x); };
   const uint32_t bOfinal = bar + 8u * (5 + 2 * NSLOT);
   const uint32_t bDrain = bar + 8u * (6 + 2 * NSLOT);
+  auto bOstaged = [&](int x) { return bar + 8u * (7 + 2 * NSLOT + x); };  // O tile x written to its ring slot
   uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + L::OFF_MISC);
   volatile uint32_t* abort_flag = misc + 1;
 
@@ -269,6 +275,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     ptx::mbar_init(bOfinal, 1);
     ptx::mbar_init(bDrain, 1);
+    ptx::mbar_init(bOstaged(0), 4);  // one arrival per softmax warp of the tile
+    ptx::mbar_init(bOstaged(1), 4);
     misc[1] = 0u;
     ptx::mbar_fence_init();
   }
@@ -289,6 +297,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::prefetch_tmap(&tmQ);
       ptx::prefetch_tmap(&tmK);
       ptx::prefetch_tmap(&tmV);
+      ptx::prefetch_tmap(&tmO);
       ptx::mbar_arrive_expect_tx(bQ, L::Q_BYTES * (w.has[1] ? 2u : 1u));
       for (int x = 0; x < 2; ++x) {
         if (!w.has[x]) continue;
@@ -492,43 +501,633 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::mbar_arrive(bPfull(x));
     }
     // ------------------------------------------------------------ epilogue
-    if (ok && nX > 0) {
+    // Once o_final has completed, every K/V load the CTA issued has been
+    // consumed, so the ring is idle: slot x stages O_X.  (Waited whenever the
+    // CTA streams any KV tile, even if this tile has none: the ring is busy
+    // until then.)
+    if (ok && n > 0) {
       ok = warp_wait_bar(bOfinal, 0, abort_flag, p.watchdog_ns, WD_SOFTMAX_O_DONE);
       if (ok) ptx::tc_fence_after();
     }
     if (ok && hasx) {
+      // O / l rounded to 16 bits, written 128-byte swizzled (the layout of a Q
+      // tile) and sent out by TMA tensor stores, one per 64-column block: the
+      // global writes are whole lines, and rows past Sq are clipped by the map.
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-      const int qrow = q0 + r;
-      const bool row_ok = qrow < p.Sq;
-      uint4* dst =
-          reinterpret_cast<uint4*>(p.o + ((static_cast<size_t>(w.b) * p.Sq + qrow) * p.Hq + hqx) * HD);
+      const uint32_t stage = sRing + x * L::SLOT_BYTES + r * 128;
+      uint32_t orr[HD];  // the whole row: all loads in flight before one wait
+      if (nX > 0) {
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
-        uint32_t orr[32];
-        if (nX > 0) {
-          ptx::tmem_ld32(tO + c * 32, orr);
-          ptx::tmem_wait_ld();
-          ptx::reg_fence(orr);
-        } else {
+        for (int c = 0; c < HD / 32; ++c) ptx::tmem_ld32(tO + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&orr[c * 32]));
+        ptx::tmem_wait_ld();
+        ptx::reg_fence(orr);
+      } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) orr[e] = 0u;
-        }
-        if (row_ok) {
+        for (int e = 0; e < HD; ++e) orr[e] = 0u;
+      }
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint4 v;
-            v.x = pack2<BF16>(__uint_as_float(orr[8 * e + 0]) * inv_l, __uint_as_float(orr[8 * e + 1]) * inv_l);
-            v.y = pack2<BF16>(__uint_as_float(orr[8 * e + 2]) * inv_l, __uint_as_float(orr[8 * e + 3]) * inv_l);
-            v.z = pack2<BF16>(__uint_as_float(orr[8 * e + 4]) * inv_l, __uint_as_float(orr[8 * e + 5]) * inv_l);
-            v.w = pack2<BF16>(__uint_as_float(orr[8 * e + 6]) * inv_l, __uint_as_float(orr[8 * e + 7]) * inv_l);
-            dst[c * 4 + e] = v;
-          }
+      for (int ch = 0; ch < HD / 8; ++ch) {  // 16-byte chunk of the row: columns 8 ch .. 8 ch + 7
+        const uint32_t* v = &orr[8 * ch];
+        ptx::st_shared_v4(stage + (ch / 8) * (BM * 128) + (((ch % 8) ^ (r % 8)) * 16),
+                          pack2<BF16>(__uint_as_float(v[0]) * inv_l, __uint_as_float(v[1]) * inv_l),
+                          pack2<BF16>(__uint_as_float(v[2]) * inv_l, __uint_as_float(v[3]) * inv_l),
+                          pack2<BF16>(__uint_as_float(v[4]) * inv_l, __uint_as_float(v[5]) * inv_l),
+                          pack2<BF16>(__uint_as_float(v[6]) * inv_l, __uint_as_float(v[7]) * inv_l));
+      }
+      ptx::fence_proxy_async_smem();  // make the generic-proxy writes visible to the TMA unit
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bOstaged(x));
+      if ((warp & 3) == 0) {
+        ok = warp_wait_bar(bOstaged(x), 0, abort_flag, p.watchdog_ns, WD_SOFTMAX_O_DONE);
+        if (ok && lane == 0) {
+#pragma unroll
+          for (int c = 0; c < (int)L::KCH; ++c)
+            ptx::tma_store_4d(&tmO, sRing + x * L::SLOT_BYTES + c * (BM * 128), c * 64, hqx, q0, w.b);
+          ptx::bulk_commit();
+          ptx::bulk_wait_read0();  // the slot must stay valid until the TMA unit has read it
         }
       }
     }
   }
 
   // ---- teardown: every role is done (or has drained); free TMEM
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ================================================ stream-K (split-KV) kernel
+//
+// The one-shot kernel above gives every CTA whole query-tile pairs, so a grid
+// with few or uneven pairs (short prompts, one head, causal rows of very
+// different lengths) leaves SMs idle and pays the pipeline fill and drain once
+// per CTA.  This kernel runs one persistent CTA per SM and cuts the whole
+// iteration space -- (query-tile pair, KV tile) steps, pairs longest first --
+// into equal contiguous ranges, one per CTA.  A pair whose steps straddle a
+// range boundary is computed in pieces: every piece after the first leaves
+// its unnormalised O, running max m and sum l in the caller's workspace and
+// raises a per-warp flag; the CTA holding the first piece (KV tile 0) waits
+// for those flags and merges the pieces in a fixed order, so results are
+// deterministic.  All CTAs of the grid are co-resident (cooperative launch),
+// and every flag wait is bounded by the watchdog.
+
+constexpr int SK_MAX_CTAS = 256;
+// The persistent loop keeps more state in the control warps than the
+// one-shot kernel: its own register split (same launch allocation).
+constexpr uint32_t SK_REGS_SOFTMAX = 200;
+constexpr uint32_t SK_REGS_CONTROL = 88;
+static_assert(128 * SK_REGS_CONTROL + 256 * SK_REGS_SOFTMAX <= NUM_THREADS * LAUNCH_REGS,
+              "register split exceeds the launch allocation");
+
+struct SkParams {
+  Params p;
+  float4* ws_o;       // partial O, float4 [SK slot][tile][HD/4][BM]
+  float* ws_ml;       // [SK slot][tile][2][BM]: m (log2 domain), l
+  unsigned* ws_flag;  // [SK slot][tile][4 warps]: == seq once that warp's rows are written
+  unsigned seq;       // this launch's sequence number (never 0)
+  int su[SK_MAX_CTAS + 1];  // CTA c starts at pair unit su[c], KV step sj[c]; it ends where CTA c+1 starts
+  int sj[SK_MAX_CTAS + 1];
+};
+
+template <int HD>
+struct SkLayout {
+  using L = Layout<HD>;
+  // The persistent CTA keeps loading the next segment's K/V while it writes
+  // the previous segment's O, so O cannot be staged in the ring: it goes
+  // through its own 32 KB stage (one 128-row x 64-column 16-bit block per
+  // query tile), paid for with one ring slot at hd 128.
+  static constexpr int NSLOT = HD == 128 ? 4 : 8;
+  static constexpr uint32_t STAGE_BYTES = BM * 128;  // one 64-column block of one tile
+  static constexpr uint32_t OFF_STAGE = L::OFF_RING + NSLOT * L::SLOT_BYTES;
+  // q_full, q_empty, full[NSLOT], empty[NSLOT], s_full[2], p_full[2], o_final[2], drain,
+  // o_staged[2], stage_free[2]
+  static constexpr uint32_t NUM_BARS = 2 + 2 * NSLOT + 2 + 2 + 2 + 1 + 2 + 2;
+  static constexpr uint32_t OFF_BAR = OFF_STAGE + 2 * STAGE_BYTES;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr uint32_t BYTES = OFF_MISC + 16;
+  static constexpr uint32_t REQUEST = BYTES + 1024;
+  static constexpr size_t WS_O_BYTES = (size_t)SK_MAX_CTAS * 2 * BM * HD * 4;
+  static constexpr size_t WS_ML_BYTES = (size_t)SK_MAX_CTAS * 2 * 2 * BM * 4;
+  static constexpr size_t WS_FLAG_BYTES = (size_t)SK_MAX_CTAS * 2 * 4 * 4;
+  static constexpr size_t WS_BYTES = WS_O_BYTES + WS_ML_BYTES + ((WS_FLAG_BYTES + 255) / 256) * 256;
+};
+
+// Geometry of pair unit u (same numbering as the one-shot grid: longest
+// first; G/2 pairs of one KV group adjacent).  Host and device share it so the
+// host's schedule and the kernel's decode cannot disagree.
+struct UnitGeo {
+  int b, hk, hq0, hq1, q00, q01;
+  bool has1;
+  int nA, nB, n;
+};
+
+__host__ __device__ __forceinline__ int geo_kv_tiles(const Params& p, int q0) {
+  const int off = p.Skv - p.Sq;
+  const int q_last = (q0 + BM < p.Sq ? q0 + BM : p.Sq) - 1;
+  int kv_hi = p.Skv;
+  if (p.causal) kv_hi = (off + q_last + 1 < p.Skv) ? off + q_last + 1 : p.Skv;
+  return kv_hi > 0 ? (kv_hi + BN - 1) / BN : 0;
+}
+
+__host__ __device__ __forceinline__ UnitGeo unit_geo(const Params& p, int u) {
+  UnitGeo w;
+  if (p.pair_heads) {
+    const int pairs = p.Hq / 2;
+    const int per_qt = pairs * p.B;
+    const int qt = p.n_qtiles - 1 - u / per_qt;
+    const int rem = u % per_qt;
+    w.b = rem / pairs;
+    const int pi = rem % pairs;
+    w.hq0 = 2 * pi;
+    w.hq1 = 2 * pi + 1;
+    w.q00 = w.q01 = qt * BM;
+    w.has1 = true;
+  } else {
+    const int npq = (p.n_qtiles + 1) / 2;
+    const int per = p.Hq * p.B;
+    const int pq = npq - 1 - u / per;
+    const int rem = u % per;
+    w.b = rem / p.Hq;
+    w.hq0 = w.hq1 = rem % p.Hq;
+    w.q00 = 2 * pq * BM;
+    w.q01 = w.q00 + BM;
+    w.has1 = w.q01 < p.Sq;
+  }
+  w.hk = w.hq0 / p.G;
+  w.nA = geo_kv_tiles(p, w.q00);
+  w.nB = w.has1 ? geo_kv_tiles(p, w.q01) : 0;
+  w.n = w.nA > w.nB ? w.nA : w.nB;
+  return w;
+}
+
+template <int HD, bool BF16>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    fa_prefill_sk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                         const __grid_constant__ SkParams sp) {
+  const Params& p = sp.p;
+  using L = Layout<HD>;
+  using SL = SkLayout<HD>;
+  constexpr int NSLOT = SL::NSLOT;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (sbase - raw);
+
+  const uint32_t sQ = sbase + L::OFF_Q;
+  const uint32_t sRing = sbase + L::OFF_RING;
+  const uint32_t bar = sbase + SL::OFF_BAR;
+  const uint32_t bQfull = bar;
+  const uint32_t bQempty = bar + 8u;
+  auto bFull = [&](int s) { return bar + 8u * (2 + s); };
+  auto bEmpty = [&](int s) { return bar + 8u * (2 + NSLOT + s); };
+  auto bSfull = [&](int x) { return bar + 8u * (2 + 2 * NSLOT + x); };
+  auto bPfull = [&](int x) { return bar + 8u * (4 + 2 * NSLOT + x); };
+  auto bOfinal = [&](int x) { return bar + 8u * (6 + 2 * NSLOT + x); };
+  const uint32_t bDrain = bar + 8u * (8 + 2 * NSLOT);
+  auto bOstaged = [&](int x) { return bar + 8u * (9 + 2 * NSLOT + x); };    // a block of O_X is in stage x
+  auto bStageFree = [&](int x) { return bar + 8u * (11 + 2 * NSLOT + x); };  // stage x has been read out
+  const uint32_t sStage = sbase + SL::OFF_STAGE;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + SL::OFF_MISC);
+  volatile uint32_t* abort_flag = misc + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int cta = static_cast<int>(blockIdx.x);
+  const int u_beg = sp.su[cta], j_beg = sp.sj[cta];
+  const int u_end = sp.su[cta + 1], j_end = sp.sj[cta + 1];
+  // the segments of this CTA: (unit u, steps [jb, je)), u from u_beg; the last
+  // one may stop before the unit's end (at the next CTA's start)
+  auto in_range = [&](int u, int jb) { return u < u_end || (u == u_end && jb < j_end); };
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bQfull, 1);
+    ptx::mbar_init(bQempty, 1);
+    for (int s = 0; s < NSLOT; ++s) {
+      ptx::mbar_init(bFull(s), 1);
+      ptx::mbar_init(bEmpty(s), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      ptx::mbar_init(bSfull(x), 1);
+      ptx::mbar_init(bPfull(x), BM);  // one arrival per softmax thread of tile x
+      ptx::mbar_init(bOfinal(x), 1);
+      ptx::mbar_init(bOstaged(x), 4);  // one arrival per softmax warp of tile x
+      ptx::mbar_init(bStageFree(x), 1);
+    }
+    ptx::mbar_init(bDrain, 1);
+    misc[1] = 0u;
+    ptx::mbar_fence_init();
+  }
+  if (warp == MMA_WARP) {
+    ptx::tmem_alloc(ptx::smem_u32(misc), TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = misc[0];
+
+  if (warp >= MMA_WARP) {
+    ptx::setmaxnreg_dec<SK_REGS_CONTROL>();
+    if (warp == PRODUCER_WARP && lane == 0) {
+      // ---------------------------------------------------------- producer
+      ptx::prefetch_tmap(&tmQ);
+      ptx::prefetch_tmap(&tmK);
+      ptx::prefetch_tmap(&tmV);
+      ptx::prefetch_tmap(&tmO);
+      int g = 0;   // loads issued into the ring
+      int nq = 0;  // segments whose Q was loaded
+      bool ok = true;
+      for (int u = u_beg, jb = j_beg; ok && in_range(u, jb); ++u, jb = 0) {
+        const UnitGeo w = unit_geo(p, u);
+        const int je = (u == u_end) ? j_end : w.n;
+        if (je <= jb) continue;  // nothing to stream (the softmax writes zeros)
+        if (nq > 0) ok = wait_bar(bQempty, (nq - 1) & 1, abort_flag, p.watchdog_ns, WD_PRODUCER_EMPTY);
+        if (!ok) break;
+        ptx::mbar_arrive_expect_tx(bQfull, L::Q_BYTES * (w.has1 ? 2u : 1u));
+#pragma unroll
+        for (int c = 0; c < (int)L::KCH; ++c)
+          ptx::tma_load_4d(sQ + c * (BM * 128), &tmQ, bQfull, c * 64, w.hq0, w.q00, w.b);
+        if (w.has1) {
+#pragma unroll
+          for (int c = 0; c < (int)L::KCH; ++c)
+            ptx::tma_load_4d(sQ + L::Q_BYTES + c * (BM * 128), &tmQ, bQfull, c * 64, w.hq1, w.q01, w.b);
+        }
+        ++nq;
+        // warm L2 with the next segment's Q: its load then waits for L2, not HBM
+        if (in_range(u + 1, 0)) {
+          const UnitGeo w2 = unit_geo(p, u + 1);
+#pragma unroll
+          for (int c = 0; c < (int)L::KCH; ++c) {
+            ptx::tma_prefetch_l2_4d(&tmQ, c * 64, w2.hq0, w2.q00, w2.b);
+            if (w2.has1) ptx::tma_prefetch_l2_4d(&tmQ, c * 64, w2.hq1, w2.q01, w2.b);
+          }
+        }
+        for (int i = 2 * jb; i < 2 * je; ++i, ++g) {
+          const int s = g % NSLOT;
+          if (g >= NSLOT) ok = wait_bar(bEmpty(s), ((g / NSLOT) & 1) ^ 1u, abort_flag, p.watchdog_ns, WD_PRODUCER_EMPTY);
+          if (!ok) break;
+          ptx::mbar_arrive_expect_tx(bFull(s), L::SLOT_BYTES);
+          const CUtensorMap* m = (i & 1) ? &tmV : &tmK;
+#pragma unroll
+          for (int c = 0; c < (int)L::KCH; ++c)
+            ptx::tma_load_4d(sRing + s * L::SLOT_BYTES + c * (BN * 128), m, bFull(s), c * 64, w.hk, (i >> 1) * BN, w.b);
+        }
+      }
+      if (!ok) {
+        if (nq > 0) drain_wait(bQfull, (nq - 1) & 1, p.watchdog_ns);
+        for (int s = 0; s < NSLOT && s < g; ++s) {
+          const int last = s + NSLOT * ((g - 1 - s) / NSLOT);
+          drain_wait(bFull(s), (last / NSLOT) & 1, p.watchdog_ns);
+        }
+      }
+    } else if (warp == MMA_WARP && lane == 0) {
+      // ------------------------------------------------------- MMA issuer
+      constexpr uint32_t IDESC_S = ptx::idesc_f16(BF16, BM, BN, false, false);
+      constexpr uint32_t IDESC_O = ptx::idesc_f16(BF16, BM, HD, false, true);
+      auto issue_s = [&](int x, int slot) {
+        const uint32_t d = tmem + L::TM_S + x * BN;
+        const uint32_t q = sQ + x * L::Q_BYTES;
+        const uint32_t k = sRing + slot * L::SLOT_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t o = (kk / 4) * (BM * 128) + (kk % 4) * 32;
+          ptx::mma_f16_ss(d, ptx::sdesc_sw128(q + o, 16, 1024), ptx::sdesc_sw128(k + o, 16, 1024), IDESC_S,
+                          kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(bSfull(x));
+      };
+      auto issue_pv = [&](int x, int slot, bool acc) {
+        const uint32_t d = tmem + L::TM_O + x * HD;
+        const uint32_t a = tmem + L::TM_S + x * BN;
+        const uint32_t v = sRing + slot * L::SLOT_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          ptx::mma_f16_ts(d, a + kk * 8, ptx::sdesc_sw128(v + kk * (16 * 128), BN * 128, 1024), IDESC_O,
+                          (acc || kk > 0) ? 1u : 0u);
+      };
+      int g = 0, nq = 0, cnt0 = 0, cnt1 = 0;
+      bool ok = true;
+      for (int u = u_beg, jb = j_beg; ok && in_range(u, jb); ++u, jb = 0) {
+        const UnitGeo w = unit_geo(p, u);
+        const int je = (u == u_end) ? j_end : w.n;
+        if (je <= jb) continue;
+        const int nseg = je - jb;
+        const int nAs = max(0, min(je, w.nA) - jb);  // tiles of A / B in this segment
+        const int nBs = max(0, min(je, w.nB) - jb);
+        ok = wait_bar(bQfull, nq & 1, abort_flag, p.watchdog_ns, WD_MMA_Q);
+        if (!ok) break;
+        const int gK = g;  // ring index of K_jb; V_(jb+t) = gK + 2t + 1, K_(jb+t) = gK + 2t
+        ok = wait_bar(bFull(gK % NSLOT), (gK / NSLOT) & 1, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        if (nAs > 0) issue_s(0, gK % NSLOT);
+        if (nBs > 0) issue_s(1, gK % NSLOT);
+        ptx::mma_commit(bEmpty(gK % NSLOT));
+        if (nseg == 1) ptx::mma_commit(bQempty);
+        for (int t = 0; ok && t < nseg; ++t) {
+          const int iv = gK + 2 * t + 1, sv = iv % NSLOT;
+          const int ik = gK + 2 * t + 2, sk = ik % NSLOT;
+          const bool more = t + 1 < nseg;
+          ok = wait_bar(bFull(sv), (iv / NSLOT) & 1, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);
+          if (!ok) break;
+          if (more) {
+            ok = wait_bar(bFull(sk), (ik / NSLOT) & 1, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);
+            if (!ok) break;
+          }
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            const int nXs = x == 0 ? nAs : nBs;
+            if (t < nXs) {
+              ok = wait_bar(bPfull(x), ((x == 0 ? cnt0 : cnt1) + t) & 1, abort_flag, p.watchdog_ns, WD_MMA_P_FULL);
+              if (!ok) break;
+              ptx::tc_fence_after();
+              issue_pv(x, sv, t > 0);
+            }
+            if (x == 1) ptx::mma_commit(bEmpty(sv));
+            if (more && t + 1 < nXs) issue_s(x, sk);
+          }
+          if (!ok) break;
+          if (more) {
+            ptx::mma_commit(bEmpty(sk));
+            if (t + 2 == nseg) ptx::mma_commit(bQempty);  // the segment's last S MMAs are issued
+          }
+        }
+        if (!ok) break;
+        if (nAs > 0) ptx::mma_commit(bOfinal(0));
+        if (nBs > 0) ptx::mma_commit(bOfinal(1));
+        g = gK + 2 * nseg;
+        cnt0 += nAs;
+        cnt1 += nBs;
+        ++nq;
+      }
+      if (!ok) {
+        ptx::mma_commit(bDrain);
+        drain_wait(bDrain, 0, p.watchdog_ns);
+      }
+    }
+  } else {
+    ptx::setmaxnreg_inc<SK_REGS_SOFTMAX>();
+    // -------------------------------------------------------------- softmax
+    const int x = warp >> 2;
+    const int r = threadIdx.x & 127;
+    const int wq = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + L::TM_S + x * BN;
+    const uint32_t tO = tmem + lane_off + L::TM_O + x * HD;
+    const int off = p.Skv - p.Sq;
+    const float sl2 = p.sl2;
+    int cnt = 0;   // tiles processed (s_full / p_full phases)
+    int ocnt = 0;  // segments with tiles of x (o_final phases)
+    int nst = 0;   // 64-column blocks of O_X sent through stage x (o_staged / stage_free phases)
+    bool ok = true;
+    // One 64-column block of O_X (this thread's row: 64 values, 32 per half)
+    // into stage x, 128-byte swizzled, then out by one TMA tensor store:
+    // whole-line global writes, rows past Sq clipped by the map.  The block
+    // before it must have been read out of the stage first.
+    const uint32_t stage_row = sStage + x * SL::STAGE_BYTES + r * 128;
+    auto stage_half = [&](int h, const float (&o)[32], float sc) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int ch = h * 4 + e;  // 16-byte chunk of the 128-byte row
+        ptx::st_shared_v4(stage_row + ((ch ^ (r % 8)) * 16), pack2<BF16>(o[8 * e + 0] * sc, o[8 * e + 1] * sc),
+                          pack2<BF16>(o[8 * e + 2] * sc, o[8 * e + 3] * sc),
+                          pack2<BF16>(o[8 * e + 4] * sc, o[8 * e + 5] * sc),
+                          pack2<BF16>(o[8 * e + 6] * sc, o[8 * e + 7] * sc));
+      }
+    };
+    auto stage_wait_free = [&]() -> bool {
+      if (nst == 0) return true;
+      return warp_wait_bar(bStageFree(x), (nst - 1) & 1, abort_flag, p.watchdog_ns, WD_SOFTMAX_O_DONE);
+    };
+    auto stage_send = [&](int cb, int hq_, int q0_, int b_) -> bool {
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bOstaged(x));
+      bool sent = true;
+      if (wq == 0) {
+        sent = warp_wait_bar(bOstaged(x), nst & 1, abort_flag, p.watchdog_ns, WD_SOFTMAX_O_DONE);
+        if (sent && lane == 0) {
+          ptx::tma_store_4d(&tmO, sStage + x * SL::STAGE_BYTES, cb * 64, hq_, q0_, b_);
+          ptx::bulk_commit();
+          ptx::bulk_wait_read0();
+          ptx::mbar_arrive(bStageFree(x));
+        }
+      }
+      ++nst;
+      return sent;
+    };
+    for (int u = u_beg, jb = j_beg; ok && in_range(u, jb); ++u, jb = 0) {
+      const UnitGeo w = unit_geo(p, u);
+      const int je = (u == u_end) ? j_end : w.n;
+      const bool first = jb == 0;
+      const bool last = je >= w.n;
+      const int q0 = x == 0 ? w.q00 : w.q01;
+      const int hqx = x == 0 ? w.hq0 : w.hq1;
+      const bool hasx = x == 0 ? true : w.has1;
+      const int nX = x == 0 ? w.nA : w.nB;
+      const int jx_end = min(je, nX);
+      const int ntile = max(0, jx_end - jb);
+      const int kv_all = p.causal ? min(p.Skv, off + q0 + 1) : p.Skv;
+      const int row_lim = p.causal ? min(p.Skv, off + q0 + r + 1) : p.Skv;
+      float m_ref = -INFINITY;
+      float l = 0.f;
+      for (int j = jb; j < jx_end; ++j, ++cnt) {
+        ok = warp_wait_bar(bSfull(x), cnt & 1, abort_flag, p.watchdog_ns, WD_SOFTMAX_S_FULL);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        uint32_t sr[BN];
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c)
+          ptx::tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+        ptx::tmem_wait_ld();
+        ptx::reg_fence(sr);
+        float s[BN];
+#pragma unroll
+        for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(sr[c]);
+        const int kv0 = j * BN;
+        if (kv0 + BN > kv_all) {
+          const int lim = row_lim - kv0;
+#pragma unroll
+          for (int c = 0; c < BN; ++c)
+            if (c >= lim) s[c] = -INFINITY;
+        }
+        float mk[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mk[k] = ptx::fmax3(s[k], s[8 + k], s[16 + k]);
+#pragma unroll
+        for (int t = 3; t < 15; t += 2)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mk[k] = ptx::fmax3(mk[k], s[8 * t + k], s[8 * t + 8 + k]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mk[k] = fmaxf(mk[k], s[120 + k]);
+        const float mx =
+            ptx::fmax3(ptx::fmax3(mk[0], mk[1], mk[2]), ptx::fmax3(mk[3], mk[4], mk[5]), fmaxf(mk[6], mk[7]));
+        const float m_new = fmaxf(m_ref, mx * sl2);
+        const bool resc = m_new > m_ref + RESCALE_TAU;
+        float alpha = 1.f;
+        if (resc) {
+          alpha = ptx::ex2(m_ref - m_new);
+          m_ref = m_new;
+          l *= alpha;
+        }
+        const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
+        const uint64_t c2 = ptx::pk(sl2, sl2);
+        const uint64_t nb2 = ptx::pk(-mb, -mb);
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+        uint32_t pp[BN / 2];
+#pragma unroll
+        for (int c = 0; c < BN; c += 2) {
+          float x0, x1;
+          ptx::upk(ptx::fma2(ptx::pk(s[c], s[c + 1]), c2, nb2), x0, x1);
+          const float e0 = ptx::ex2(x0), e1 = ptx::ex2(x1);
+          acc[(c >> 1) & 3] = ptx::add2(acc[(c >> 1) & 3], ptx::pk(e0, e1));
+          pp[c >> 1] = pack2<BF16>(e0, e1);
+        }
+        {
+          float a0, a1;
+          ptx::upk(ptx::add2(ptx::add2(acc[0], acc[1]), ptx::add2(acc[2], acc[3])), a0, a1);
+          l += a0 + a1;
+        }
+        if (j > jb && __any_sync(0xffffffffu, resc)) {
+          const uint64_t a2 = ptx::pk(alpha, alpha);
+#pragma unroll
+          for (int c = 0; c < HD / 32; ++c) {
+            uint32_t orr[32];
+            ptx::tmem_ld32(tO + c * 32, orr);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence(orr);
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              float o0, o1;
+              ptx::upk(ptx::mul2(ptx::pk(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])), a2), o0, o1);
+              orr[e] = __float_as_uint(o0);
+              orr[e + 1] = __float_as_uint(o1);
+            }
+            ptx::tmem_st32(tO + c * 32, orr);
+          }
+        }
+        ptx::tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pp[0]));
+        ptx::tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pp[32]));
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bPfull(x));
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      if (ntile > 0) {
+        ok = warp_wait_bar(bOfinal(x), ocnt & 1, abort_flag, p.watchdog_ns, WD_SOFTMAX_O_DONE);
+        if (!ok) break;
+        ++ocnt;
+        ptx::tc_fence_after();
+      }
+      if (!hasx) continue;
+      const size_t slot_t = static_cast<size_t>(cta) * 2 + x;  // this CTA's workspace slot, tile x
+      if (!first) {
+        // a later piece of this pair: leave (O, m, l) for the CTA holding KV tile 0
+        if (ntile > 0) {
+          float4* dst = sp.ws_o + slot_t * (HD / 4) * BM + r;
+#pragma unroll
+          for (int c = 0; c < HD / 32; ++c) {
+            uint32_t orr[32];
+            ptx::tmem_ld32(tO + c * 32, orr);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence(orr);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              dst[(c * 8 + e) * BM] = make_float4(__uint_as_float(orr[4 * e]), __uint_as_float(orr[4 * e + 1]),
+                                                  __uint_as_float(orr[4 * e + 2]), __uint_as_float(orr[4 * e + 3]));
+          }
+        }
+        sp.ws_ml[(slot_t * 2 + 0) * BM + r] = ntile > 0 ? m_ref : -INFINITY;
+        sp.ws_ml[(slot_t * 2 + 1) * BM + r] = ntile > 0 ? l : 0.f;
+        __syncwarp();
+        if (lane == 0) ptx::st_release_gpu(sp.ws_flag + slot_t * 4 + wq, sp.seq);
+        continue;
+      }
+      // KV tile 0 is here: this CTA writes the output, merging the later pieces
+      // (CTAs cta+1, cta+2, ... whose ranges start inside this pair) in order
+      float M = ntile > 0 ? m_ref : -INFINITY;
+      int kend = cta + 1;
+      if (!last) {
+        while (kend < static_cast<int>(gridDim.x) && sp.su[kend] == u) ++kend;
+        for (int k = cta + 1; ok && k < kend; ++k) {
+          const unsigned* f = sp.ws_flag + (static_cast<size_t>(k) * 2 + x) * 4 + wq;
+          bool got = ptx::ld_acquire_gpu(f) == sp.seq;
+          if (!got) {
+            const uint64_t t0 = ptx::globaltimer_ns();
+            while (!got) {
+              __nanosleep(128);
+              got = ptx::ld_acquire_gpu(f) == sp.seq;
+              if (!got && (*abort_flag || ptx::globaltimer_ns() - t0 > p.watchdog_ns)) {
+                if (!*abort_flag) {
+                  *abort_flag = 1u;
+                  const uint32_t ci = blockIdx.x < 0xFFFFFFu ? blockIdx.x : 0xFFFFFFu;
+                  atomicCAS(&g_fa_status, 0u, (WD_MERGE_FLAG & 0xFFu) | (ci << 8));
+                }
+                break;
+              }
+            }
+          }
+          ok = __all_sync(0xffffffffu, got);
+          if (ok) M = fmaxf(M, sp.ws_ml[((static_cast<size_t>(k) * 2 + x) * 2 + 0) * BM + r]);
+        }
+        if (!ok) break;
+      }
+      const float fs = (ntile > 0 && m_ref != -INFINITY) ? ptx::ex2(m_ref - M) : 0.f;
+      float Lsum = (ntile > 0) ? l * fs : 0.f;
+      for (int k = cta + 1; k < kend; ++k) {
+        const float mk_ = sp.ws_ml[((static_cast<size_t>(k) * 2 + x) * 2 + 0) * BM + r];
+        const float lk = sp.ws_ml[((static_cast<size_t>(k) * 2 + x) * 2 + 1) * BM + r];
+        if (mk_ != -INFINITY) Lsum += lk * ptx::ex2(mk_ - M);
+      }
+      const float inv_l = (Lsum > 0.f) ? 1.f / Lsum : 0.f;
+#pragma unroll
+      for (int cb = 0; cb < (int)L::KCH; ++cb) {
+        ok = stage_wait_free();
+        if (!ok) break;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int c = cb * 2 + h;  // 32-column piece
+          float o[32];
+          if (ntile > 0) {
+            uint32_t orr[32];
+            ptx::tmem_ld32(tO + c * 32, orr);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence(orr);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(orr[e]) * fs;
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = 0.f;
+          }
+          for (int k = cta + 1; k < kend; ++k) {
+            const float mk_ = sp.ws_ml[((static_cast<size_t>(k) * 2 + x) * 2 + 0) * BM + r];
+            if (mk_ == -INFINITY) continue;
+            const float fk = ptx::ex2(mk_ - M);
+            const float4* srcp = sp.ws_o + (static_cast<size_t>(k) * 2 + x) * (HD / 4) * BM + r;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float4 v4 = srcp[(c * 8 + e) * BM];
+              o[4 * e + 0] += v4.x * fk;
+              o[4 * e + 1] += v4.y * fk;
+              o[4 * e + 2] += v4.z * fk;
+              o[4 * e + 3] += v4.w * fk;
+            }
+          }
+          stage_half(h, o, inv_l);
+        }
+        ok = stage_send(cb, hqx, q0, w.b);
+        if (!ok) break;
+      }
+      if (!ok) break;
+    }
+  }
+
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == MMA_WARP) {
@@ -580,11 +1179,20 @@ static long long grid_size(int B, int Hq, int Hkv, int Sq) {
   return ((n_qt + 1) / 2) * Hq * (long long)B;
 }
 
+// Pair units of a launch (the one-shot kernel's grid size).
+static long long unit_count_of(const Params& p) {
+  const long long n_qt = p.n_qtiles;
+  if (p.pair_heads) return n_qt * (p.Hq / 2) * p.B;
+  return ((n_qt + 1) / 2) * (long long)p.Hq * p.B;
+}
+
 constexpr int MAX_DEVICES = 64;
 
 // Per-device facts, filled once: 1 = sm_103 with enough opt-in shared memory.
 static std::atomic<int> g_dev_ok[MAX_DEVICES];
+static std::atomic<int> g_dev_sms[MAX_DEVICES];
 static std::atomic<int> g_attr_set[MAX_DEVICES][4];
+static std::atomic<int> g_sk_attr_set[MAX_DEVICES][4];
 
 static int check_device(int* dev_out) {
   int dev = -1;
@@ -595,15 +1203,17 @@ static int check_device(int* dev_out) {
   *dev_out = dev;
   int st = g_dev_ok[dev].load();
   if (st == 0) {
-    int major = 0, minor = 0, optin = 0;
+    int major = 0, minor = 0, optin = 0, sms = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
       (void)cudaGetLastError();
       return FA_ERR_DEVICE;
     }
+    g_dev_sms[dev].store(sms > 0 ? sms : 1);
     if (major != 10 || minor != 3) st = -FA_ERR_DEVICE;
-    else if ((unsigned)optin < Layout<128>::REQUEST) st = -FA_ERR_SMEM;
+    else if ((unsigned)optin < Layout<128>::REQUEST || (unsigned)optin < SkLayout<128>::REQUEST) st = -FA_ERR_SMEM;
     else st = 1;
     g_dev_ok[dev].store(st);
   }
@@ -630,9 +1240,9 @@ static int launch(const void* q, const void* k, const void* v, void* o, int B, i
   }
   EncodeTiledFn enc = encoder();
   if (!enc) return FA_ERR_LAUNCH;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, HD) || !encode_bshd(&mk, enc, k, BF16, B, Skv, Hkv, HD) ||
-      !encode_bshd(&mv, enc, v, BF16, B, Skv, Hkv, HD))
+      !encode_bshd(&mv, enc, v, BF16, B, Skv, Hkv, HD) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, HD))
     return FA_ERR_LAUNCH;
   Params prm;
   prm.o = static_cast<uint16_t*>(o);
@@ -648,21 +1258,27 @@ static int launch(const void* q, const void* k, const void* v, void* o, int B, i
   prm.sl2 = scale * 1.4426950408889634f;
   prm.watchdog_ns = WATCHDOG_NS;
   const long long grid = grid_size(B, Hq, Hkv, Sq);
-  kern<<<dim3((unsigned)grid), dim3(NUM_THREADS), L::REQUEST, stream>>>(mq, mk, mv, prm);
+  kern<<<dim3((unsigned)grid), dim3(NUM_THREADS), L::REQUEST, stream>>>(mq, mk, mv, mo, prm);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   return FA_OK;
 }
 
-static int run(bool bf16, const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int Sq,
-               int Skv, int hd, int causal, float scale, void* stream) {
+// Argument checks shared by every entry point (no device call).  May replace
+// k and v by q when Skv == 0 (no key is ever loaded; the maps need a base).
+static int validate(const void* q, const void*& k, const void*& v, const void* o, int B, int Hq, int Hkv, int Sq,
+                    int Skv, int hd, float scale, bool* empty) {
+  *empty = false;
   if (B < 0 || Sq < 0 || Skv < 0 || Hq < 1 || Hkv < 1) return FA_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (hd != 64 && hd != 128) return FA_ERR_UNSUPPORTED;
-  if (B == 0 || Sq == 0) return FA_OK;  // nothing to compute; no pointer is read
+  if (B == 0 || Sq == 0) {  // nothing to compute; no pointer is read
+    *empty = true;
+    return FA_OK;
+  }
   if (!q || !o) return FA_ERR_INVALID_ARG;
   if (Skv > 0 && (!k || !v)) return FA_ERR_INVALID_ARG;
-  if (Skv == 0) k = v = q;  // no key is ever loaded; the K/V maps only need a valid base
+  if (Skv == 0) k = v = q;
   const auto mis = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15u) != 0; };
   if (mis(q) || mis(k) || mis(v) || mis(o)) return FA_ERR_ALIGNMENT;
   // TMA coordinates are 32-bit and a box may start up to 127 rows past the end.
@@ -675,6 +1291,14 @@ static int run(bool bf16, const void* q, const void* k, const void* v, void* o, 
   if (overlaps(o, qn * 2, q, qn * 2) || overlaps(o, qn * 2, k, kn * 2) || overlaps(o, qn * 2, v, kn * 2))
     return FA_ERR_INVALID_ARG;
   if (grid_size(B, Hq, Hkv, Sq) > 0x7FFFFFFFLL) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+static int run(bool bf16, const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int Sq,
+               int Skv, int hd, int causal, float scale, void* stream) {
+  bool empty = false;
+  const int vs = validate(q, k, v, o, B, Hq, Hkv, Sq, Skv, hd, scale, &empty);
+  if (vs != FA_OK || empty) return vs;
   int dev = -1;
   const int ds = check_device(&dev);
   if (ds != FA_OK) return ds;
@@ -684,6 +1308,177 @@ static int run(bool bf16, const void* q, const void* k, const void* v, void* o, 
                 : launch<128, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, causal, scale, st, dev);
   return bf16 ? launch<64, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, causal, scale, st, dev)
               : launch<64, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, causal, scale, st, dev);
+}
+
+// ------------------------------------------------------ stream-K host side
+
+static size_t ws_bytes_for(int hd) {
+  if (hd == 128) return SkLayout<128>::WS_BYTES;
+  if (hd == 64) return SkLayout<64>::WS_BYTES;
+  return 0;
+}
+
+// The per-CTA starting points of an even split of all (pair, KV step) steps
+// over the grid.  Cached per shape: the scan over pairs runs once per shape.
+struct SkSchedule {
+  int key[7];
+  int G;
+  int su[SK_MAX_CTAS + 1];
+  int sj[SK_MAX_CTAS + 1];
+};
+
+static std::mutex g_sched_mu;
+static SkSchedule g_sched_cache[8];
+static int g_sched_n = 0, g_sched_next = 0;
+
+// Cost model of the schedule, in quarter KV steps: a segment (one unit, or a
+// piece of one) costs its KV steps plus a fixed part for its Q load, its O
+// epilogue and, for a split unit, the partial write and the merge.  Pieces
+// shorter than SK_MIN_PIECE steps are not cut: the boundary moves to the
+// nearer unit edge.
+constexpr int SK_SEG_COST_Q = 8;  // fixed cost of a segment: two KV steps
+constexpr int SK_MIN_PIECE = 2;
+
+static void make_schedule(const Params& prm, int sms, SkSchedule* sc) {
+  const long long nu = unit_count_of(prm);
+  std::vector<int> n(static_cast<size_t>(nu));
+  long long T = 0;  // total cost, quarter steps
+  for (long long u = 0; u < nu; ++u) {
+    n[u] = unit_geo(prm, static_cast<int>(u)).n;
+    T += 4LL * n[u] + SK_SEG_COST_Q;
+  }
+  const int want = static_cast<int>(std::max<long long>(1, std::min<long long>(std::min(sms, SK_MAX_CTAS), nu * 64)));
+  // CTA c starts at cost T c / want, rounded to a (unit, step) boundary;
+  // boundaries strictly increase, so no CTA's range is empty
+  int G = 1;
+  sc->su[0] = 0;
+  sc->sj[0] = 0;
+  long long acc = 0;  // cost of units [0, u)
+  int u = 0;
+  for (int c = 1; c < want; ++c) {
+    const long long target = T * c / want;
+    while (u < nu && acc + 4LL * n[u] + SK_SEG_COST_Q <= target) acc += 4LL * n[u++] + SK_SEG_COST_Q;
+    if (u >= nu) break;
+    const long long j = (target - acc - SK_SEG_COST_Q) / 4;  // KV steps into unit u (may be negative)
+    int bu = u, bj;
+    if (j < SK_MIN_PIECE) {
+      bj = 0;
+    } else if (n[u] - j < SK_MIN_PIECE) {
+      bu = u + 1;
+      bj = 0;
+    } else {
+      bj = static_cast<int>(j);
+    }
+    if (bu >= nu) break;
+    if (bu > sc->su[G - 1] || (bu == sc->su[G - 1] && bj > sc->sj[G - 1])) {
+      sc->su[G] = bu;
+      sc->sj[G] = bj;
+      ++G;
+    }
+  }
+  sc->G = G;
+  sc->su[G] = static_cast<int>(nu);
+  sc->sj[G] = 0;
+}
+
+static void get_schedule(const Params& prm, int sms, SkSchedule* out) {
+  const int key[7] = {prm.B, prm.Hq, prm.Hkv, prm.Sq, prm.Skv, prm.causal, sms};
+  std::lock_guard<std::mutex> lk(g_sched_mu);
+  for (int i = 0; i < g_sched_n; ++i)
+    if (std::memcmp(g_sched_cache[i].key, key, sizeof(key)) == 0) {
+      *out = g_sched_cache[i];
+      return;
+    }
+  SkSchedule& sc = g_sched_cache[g_sched_next];
+  std::memcpy(sc.key, key, sizeof(key));
+  make_schedule(prm, sms, &sc);
+  *out = sc;
+  g_sched_next = (g_sched_next + 1) % 8;
+  if (g_sched_n < 8) ++g_sched_n;
+}
+
+static std::atomic<unsigned> g_seq{0};
+
+template <int HD, bool BF16>
+static int launch_sk(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int Sq, int Skv,
+                     int causal, float scale, void* ws, cudaStream_t stream, int dev) {
+  using SL = SkLayout<HD>;
+  auto kern = fa_prefill_sk_kernel<HD, BF16>;
+  const int slot = (HD == 128 ? 2 : 0) + (BF16 ? 1 : 0);
+  if (g_sk_attr_set[dev][slot].load() == 0) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SL::REQUEST) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return FA_ERR_SMEM;
+    }
+    g_sk_attr_set[dev][slot].store(1);
+  }
+  EncodeTiledFn enc = encoder();
+  if (!enc) return FA_ERR_LAUNCH;
+  CUtensorMap mq, mk, mv, mo;
+  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, HD) || !encode_bshd(&mk, enc, k, BF16, B, Skv, Hkv, HD) ||
+      !encode_bshd(&mv, enc, v, BF16, B, Skv, Hkv, HD) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, HD))
+    return FA_ERR_LAUNCH;
+  SkParams sp;
+  std::memset(&sp, 0, sizeof(sp));
+  Params& prm = sp.p;
+  prm.o = static_cast<uint16_t*>(o);
+  prm.B = B;
+  prm.Hq = Hq;
+  prm.Hkv = Hkv;
+  prm.Sq = Sq;
+  prm.Skv = Skv;
+  prm.G = Hq / Hkv;
+  prm.n_qtiles = (Sq + BM - 1) / BM;
+  prm.pair_heads = (prm.G % 2 == 0) ? 1 : 0;
+  prm.causal = causal ? 1 : 0;
+  prm.sl2 = scale * 1.4426950408889634f;
+  prm.watchdog_ns = WATCHDOG_NS;
+  SkSchedule sc;
+  get_schedule(prm, g_dev_sms[dev].load(), &sc);
+  std::memcpy(sp.su, sc.su, sizeof(int) * (sc.G + 1));
+  std::memcpy(sp.sj, sc.sj, sizeof(int) * (sc.G + 1));
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  sp.ws_o = reinterpret_cast<float4*>(base);
+  sp.ws_ml = reinterpret_cast<float*>(base + SL::WS_O_BYTES);
+  sp.ws_flag = reinterpret_cast<unsigned*>(base + SL::WS_O_BYTES + SL::WS_ML_BYTES);
+  unsigned seq = ++g_seq;
+  if (seq == 0) seq = ++g_seq;
+  sp.seq = seq;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(static_cast<unsigned>(sc.G));
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = SL::REQUEST;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident: merges wait on other CTAs
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, sp) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return FA_ERR_LAUNCH;
+  }
+  return FA_OK;
+}
+
+static int run_ws(bool bf16, const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int Sq,
+                  int Skv, int hd, int causal, float scale, void* ws, size_t ws_bytes, void* stream) {
+  bool empty = false;
+  const int vs = validate(q, k, v, o, B, Hq, Hkv, Sq, Skv, hd, scale, &empty);
+  if (vs != FA_OK || empty) return vs;
+  if (!ws) return FA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return FA_ERR_ALIGNMENT;
+  if (ws_bytes < ws_bytes_for(hd)) return FA_ERR_INVALID_ARG;
+  int dev = -1;
+  const int ds = check_device(&dev);
+  if (ds != FA_OK) return ds;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (hd == 128)
+    return bf16 ? launch_sk<128, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, causal, scale, ws, st, dev)
+                : launch_sk<128, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, causal, scale, ws, st, dev);
+  return bf16 ? launch_sk<64, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, causal, scale, ws, st, dev)
+              : launch_sk<64, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, causal, scale, ws, st, dev);
 }
 
 }  // namespace fa
@@ -699,6 +1494,20 @@ extern "C" int fa_prefill_bf16(const void* q, const void* k, const void* v, void
                                int Skv, int hd, int causal, float scale, void* stream) {
   return fa::run(true, q, k, v, o, B, Hq, Hkv, Sq, Skv, hd, causal, scale, stream);
 }
+
+extern "C" int fa_prefill_ws(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int Sq,
+                             int Skv, int hd, int causal, float scale, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  return fa::run_ws(false, q, k, v, o, B, Hq, Hkv, Sq, Skv, hd, causal, scale, workspace, workspace_bytes, stream);
+}
+
+extern "C" int fa_prefill_ws_bf16(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
+                                  int Sq, int Skv, int hd, int causal, float scale, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  return fa::run_ws(true, q, k, v, o, B, Hq, Hkv, Sq, Skv, hd, causal, scale, workspace, workspace_bytes, stream);
+}
+
+extern "C" size_t fa_workspace_bytes(int hd) { return fa::ws_bytes_for(hd); }
 
 extern "C" const char* fa_status_string(int status) {
   switch (status) {

@@ -60,6 +60,8 @@
 #ifndef FA_PREFILL_H
 #define FA_PREFILL_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -97,6 +99,47 @@ int fa_prefill(const void* q, const void* k, const void* v, void* o,
 int fa_prefill_bf16(const void* q, const void* k, const void* v, void* o,
                     int B, int Hq, int Hkv, int Sq, int Skv, int hd,
                     int causal, float scale, void* stream);
+
+/*
+ * fa_prefill_ws / fa_prefill_ws_bf16 -- the same operation computed by a
+ * persistent, load-balanced ("stream-K" / split-KV) kernel: one CTA per SM,
+ * each taking an equal share of all (query-tile pair, KV tile) steps, so short
+ * prompts, single heads and causal rows of very different lengths keep every
+ * SM busy.  A query-tile pair whose KV steps are split between CTAs is merged
+ * in a fixed order (results are deterministic, run to run); this is the
+ * split-K with a fixed-order reduction and no atomic accumulation that the
+ * pages' GEMM work uses for underfilled grids, applied to the KV dimension.
+ * The merge keeps each piece's unnormalised O with its running max m and sum
+ * l, the state of the online softmax (minfer "53 · r50 — FA_TKV 32->16
+ * occupancy experiment", section 2), and combines pieces exactly as the
+ * online softmax combines tiles.
+ *
+ * The first 13 arguments are those of fa_prefill / fa_prefill_bf16, then:
+ *   workspace        caller-owned DEVICE memory, >= fa_workspace_bytes(hd)
+ *                    bytes, 256-byte aligned, ZERO-FILLED before its first use
+ *                    (the library keeps it consistent afterwards: each call
+ *                    tags what it writes with a fresh sequence number)
+ *   workspace_bytes  its size in bytes
+ * Calls that share one workspace must not overlap on the GPU (issue them on
+ * one stream, or give each stream its own workspace).  The kernel is launched
+ * cooperatively (all its CTAs resident at once); if the device cannot hold
+ * the grid the call returns FA_ERR_LAUNCH.
+ * Additional errors: FA_ERR_INVALID_ARG for a NULL or too small workspace,
+ * FA_ERR_ALIGNMENT for a workspace not 256-byte aligned.
+ */
+int fa_prefill_ws(const void* q, const void* k, const void* v, void* o,
+                  int B, int Hq, int Hkv, int Sq, int Skv, int hd,
+                  int causal, float scale, void* workspace,
+                  size_t workspace_bytes, void* stream);
+
+int fa_prefill_ws_bf16(const void* q, const void* k, const void* v, void* o,
+                       int B, int Hq, int Hkv, int Sq, int Skv, int hd,
+                       int causal, float scale, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/* Workspace bytes fa_prefill_ws needs for head dimension hd (0 if
+ * unsupported); independent of the other sizes.  Host-only. */
+size_t fa_workspace_bytes(int hd);
 
 /* A static, human-readable name for a status code (never NULL). */
 const char* fa_status_string(int status);

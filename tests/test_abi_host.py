@@ -28,8 +28,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("fa_prefill", "fa_prefill_bf16", "fa_status_string", "fa_smem_bytes",
-              "fa_debug_status", "fa_debug_status_clear"):
+    for n in ("fa_prefill", "fa_prefill_bf16", "fa_prefill_ws", "fa_prefill_ws_bf16", "fa_workspace_bytes",
+              "fa_status_string", "fa_smem_bytes", "fa_debug_status", "fa_debug_status_clear"):
         assert n in names
 
 
@@ -53,7 +53,7 @@ def test_smem_request_matches_the_tile_layout(fa):
     for hd, nslot in ((64, 8), (128, 5)):
         q = 128 * hd * 2
         slot = 128 * hd * 2
-        bars = 1 + 2 * nslot + 2 + 2 + 2
+        bars = 1 + 2 * nslot + 2 + 2 + 2 + 2  # + o_staged[2]
         want = 2 * q + nslot * slot + bars * 8 + 16 + 1024
         assert fa.smem_bytes(hd) == want
         assert want <= 227 * 1024
@@ -92,3 +92,22 @@ def test_python_wrapper_rejects_cpu_tensors(fa):
     q = torch.zeros((1, 4, 2, 128), dtype=torch.float16)
     with pytest.raises(ValueError):
         fa.attention(q, q, q)
+
+
+def test_workspace_size_and_errors_without_a_device(fa):
+    """Stream-K workspace: per SM slot (up to 256), both tiles' partial O in f32
+    plus m and l per row, plus one flag per (tile, warp)."""
+    for hd in (64, 128):
+        o_bytes = 256 * 2 * 128 * hd * 4
+        ml_bytes = 256 * 2 * 2 * 128 * 4
+        flag_bytes = ((256 * 2 * 4 * 4 + 255) // 256) * 256
+        assert fa.workspace_bytes(hd) == o_bytes + ml_bytes + flag_bytes
+    assert fa.workspace_bytes(80) == 0
+    ws = fa.workspace_bytes(128)
+    args = (A, 2 * A, 3 * A, 4 * A, 1, 4, 2, 8, 8, 128, 1, 0.1)
+    for f in (fa.fa_prefill_ws, fa.fa_prefill_ws_bf16):
+        assert f(*args, 0, ws, 0) == 1                # no workspace
+        assert f(*args, 5 * A + 16, ws, 0) == 3       # not 256-byte aligned
+        assert f(*args, 5 * A, ws - 1, 0) == 1        # too small
+        assert f(A, 2 * A, 3 * A, 4 * A, 0, 4, 2, 8, 8, 128, 1, 0.1, 0, 0, 0) == 0  # empty problem: no-op
+        assert f(A, 2 * A, 3 * A, 4 * A, 1, 4, 2, 8, 8, 96, 1, 0.1, 5 * A, ws, 0) == 2

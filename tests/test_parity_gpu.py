@@ -43,11 +43,17 @@ def _inputs(B, Hq, Hkv, Sq, Skv, hd, dtype="f16", seed=0, q_std=1.0, k_std=1.0, 
     return w, W.make_inputs(w)
 
 
-def _run_gpu(q, k, v, causal, scale, fill=float("nan")):
+@pytest.fixture(params=[False, True], ids=["oneshot", "streamk"])
+def split(request):
+    """Run a parity test through the one-shot kernel and the stream-K kernel."""
+    return request.param
+
+
+def _run_gpu(q, k, v, causal, scale, fill=float("nan"), split=False):
     fa = _fa()
     dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
     out = torch.full_like(dq, fill)  # NaN-prefilled: an unwritten element fails parity
-    fa.attention(dq, dk, dv, causal=causal, scale=scale, out=out)
+    fa.attention(dq, dk, dv, causal=causal, scale=scale, out=out, split=split)
     torch.cuda.synchronize()
     assert fa.debug_status() == 0, f"kernel watchdog fired: {fa.debug_status():#x}"
     return out.cpu()
@@ -66,9 +72,9 @@ def _check(got, want, dtype, what=""):
     return float(np.max(err)) if err.size else 0.0
 
 
-def _full_case(B, Hq, Hkv, Sq, Skv, hd, causal=True, dtype="f16", seed=0, **std):
+def _full_case(B, Hq, Hkv, Sq, Skv, hd, causal=True, dtype="f16", seed=0, split=False, **std):
     w, (q, k, v) = _inputs(B, Hq, Hkv, Sq, Skv, hd, dtype, seed, **std)
-    got = _run_gpu(q, k, v, causal, w.scale)
+    got = _run_gpu(q, k, v, causal, w.scale, split=split)
     want = oracle.attention(q, k, v, causal=causal, scale=w.scale)
     return _check(got, want, dtype, f"B{B} H{Hq}/{Hkv} Sq{Sq} Skv{Skv} hd{hd} causal{causal} {dtype}")
 
@@ -78,27 +84,27 @@ def _full_case(B, Hq, Hkv, Sq, Skv, hd, causal=True, dtype="f16", seed=0, **std)
 @pytest.mark.parametrize("hd", [64, 128])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("S", [1, 2, 3, 127, 128, 129, 255, 256, 300])
-def test_square_causal_lengths(S, dtype, hd):
-    _full_case(1, 2, 1, S, S, hd, True, dtype, seed=S)
+def test_square_causal_lengths(S, dtype, hd, split):
+    _full_case(1, 2, 1, S, S, hd, True, dtype, seed=S, split=split)
 
 
 @pytest.mark.parametrize("Sq,Skv", [(1, 129), (64, 200), (129, 1000), (200, 513), (384, 385)])
 @pytest.mark.parametrize("hd", [64, 128])
-def test_chunked_bottom_right(Sq, Skv, hd):
-    _full_case(2, 4, 2, Sq, Skv, hd, True, "f16", seed=Sq + Skv)
+def test_chunked_bottom_right(Sq, Skv, hd, split):
+    _full_case(2, 4, 2, Sq, Skv, hd, True, "f16", seed=Sq + Skv, split=split)
 
 
 @pytest.mark.parametrize("Sq,Skv", [(129, 255), (300, 128), (5, 700), (256, 256)])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-def test_non_causal(Sq, Skv, dtype):
-    _full_case(1, 4, 4, Sq, Skv, 128, False, dtype, seed=7)
+def test_non_causal(Sq, Skv, dtype, split):
+    _full_case(1, 4, 4, Sq, Skv, 128, False, dtype, seed=7, split=split)
 
 
 @pytest.mark.parametrize("Sq,Skv", [(300, 40), (256, 129), (130, 1)])
-def test_rows_with_no_visible_key_are_zero(Sq, Skv):
+def test_rows_with_no_visible_key_are_zero(Sq, Skv, split):
     """causal with Skv < Sq: rows i < Sq - Skv see no key and must be exactly 0."""
     w, (q, k, v) = _inputs(1, 2, 2, Sq, Skv, 128, "f16", 3)
-    got = _run_gpu(q, k, v, True, w.scale)
+    got = _run_gpu(q, k, v, True, w.scale, split=split)
     want = oracle.attention(q, k, v, causal=True, scale=w.scale)
     _check(got, want, "f16", "masked rows")
     n0 = Sq - Skv
@@ -106,16 +112,17 @@ def test_rows_with_no_visible_key_are_zero(Sq, Skv):
 
 
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
-def test_gqa_groups(G):
-    _full_case(2, 8, 8 // G, 257, 257, 128, True, "bf16", seed=G)
+def test_gqa_groups(G, split):
+    _full_case(2, 8, 8 // G, 257, 257, 128, True, "bf16", seed=G, split=split)
 
 
 @pytest.mark.parametrize("std", [3.0, 10.0])
-def test_large_score_ranges(std):
+def test_large_score_ranges(std, split):
     """Scores with std 9 and 100: the online max subtraction and the lazy
-    rescale must keep everything finite and exact to tolerance."""
-    _full_case(1, 4, 4, 400, 400, 128, True, "f16", seed=int(std), q_std=std, k_std=std)
-    _full_case(1, 4, 4, 400, 400, 64, True, "bf16", seed=int(std), q_std=std, k_std=std)
+    rescale (and, split, the merge of pieces with different maxima) must keep
+    everything finite and exact to tolerance."""
+    _full_case(1, 4, 4, 400, 400, 128, True, "f16", seed=int(std), split=split, q_std=std, k_std=std)
+    _full_case(1, 4, 4, 400, 400, 64, True, "bf16", seed=int(std), split=split, q_std=std, k_std=std)
 
 
 def test_scale_is_applied():
@@ -224,7 +231,7 @@ def test_runs_on_a_side_stream():
 # ------------------------------------------------------------ the six workloads
 
 @pytest.mark.parametrize("idx", range(len(W.WORKLOADS)))
-def test_workload_reduced_full_compare(idx):
+def test_workload_reduced_full_compare(idx, split):
     """Each workload's structure (dtype, GQA ratio, std, chunk offset, hd) at a
     size the oracle finishes in seconds, spanning several tiles and a ragged tail."""
     w = W.WORKLOADS[idx]
@@ -235,19 +242,19 @@ def test_workload_reduced_full_compare(idx):
     else:  # chunked: keep the offset structure (Skv - Sq >> Sq) at a smaller size
         small = w.with_(B=2, Hq=8, Hkv=2, Sq=160, Skv=1184)
     q, k, v = W.make_inputs(small)
-    got = _run_gpu(q, k, v, small.causal, small.scale)
+    got = _run_gpu(q, k, v, small.causal, small.scale, split=split)
     want = oracle.attention(q, k, v, causal=small.causal, scale=small.scale)
     _check(got, want, small.dtype, small.name)
 
 
 @pytest.mark.parametrize("idx", range(len(W.WORKLOADS)))
-def test_workload_full_size_sampled_rows(idx):
+def test_workload_full_size_sampled_rows(idx, split):
     """The workload at its full size, in the benchmark's launch configuration:
     a sample of output rows (always the first/last rows of the first/last heads)
     against the oracle computed row by row; plus whole-tensor properties."""
     w = W.WORKLOADS[idx]
     q, k, v = W.make_inputs(w)
-    got = _run_gpu(q, k, v, w.causal, w.scale)
+    got = _run_gpu(q, k, v, w.causal, w.scale, split=split)
     assert torch.isfinite(got).all()
     rows = W.sample_rows(w, 384 if w.Skv >= 4096 else 768)
     want = oracle.attention_rows(q, k, v, rows.numpy(), causal=w.causal, scale=w.scale)
@@ -262,9 +269,9 @@ def test_workload_full_size_sampled_rows(idx):
 
 # ------------------------------------------------------ many-CTA / sparse grids
 
-def _sampled_case(B, Hq, Hkv, Sq, Skv, hd, dtype, seed, causal=True, n_rows=512):
+def _sampled_case(B, Hq, Hkv, Sq, Skv, hd, dtype, seed, causal=True, n_rows=512, split=False):
     w, (q, k, v) = _inputs(B, Hq, Hkv, Sq, Skv, hd, dtype, seed)
-    got = _run_gpu(q, k, v, causal, w.scale)
+    got = _run_gpu(q, k, v, causal, w.scale, split=split)
     rows = W.sample_rows(w, n_rows, seed=seed)
     want = oracle.attention_rows(q, k, v, rows.numpy(), causal=causal, scale=w.scale)
     g = got[rows[:, 0].long(), rows[:, 2].long(), rows[:, 1].long()]
@@ -272,21 +279,62 @@ def _sampled_case(B, Hq, Hkv, Sq, Skv, hd, dtype, seed, causal=True, n_rows=512)
     return got, rows
 
 
-def test_many_units_with_empty_ones_between():
+def test_many_units_with_empty_ones_between(split):
     """Many more CTAs than SMs, most of them with no visible key (causal,
     Skv << Sq): CTAs with nothing to stream write zeros, and every row before
     Sq - Skv must come out exactly 0."""
     Sq, Skv = 8192, 1000
-    got, _ = _sampled_case(1, 40, 40, Sq, Skv, 128, "f16", 21)
+    got, _ = _sampled_case(1, 40, 40, Sq, Skv, 128, "f16", 21, split=split)
     assert torch.all(got[:, : Sq - Skv] == 0)
     assert torch.isfinite(got).all()
 
 
-def test_odd_gqa_group_pairs_row_tiles_over_rounds():
+def test_odd_gqa_group_pairs_row_tiles_over_rounds(split):
     """G = 3 (odd): a CTA pairs two row tiles of one head (the second may be
     past Sq); B = 4 gives several waves of CTAs."""
-    _sampled_case(4, 12, 4, 1000, 1000, 128, "bf16", 22)
+    _sampled_case(4, 12, 4, 1000, 1000, 128, "bf16", 22, split=split)
 
 
-def test_even_gqa_many_rounds_hd64():
-    _sampled_case(2, 16, 4, 3000, 3000, 64, "f16", 23)
+def test_even_gqa_many_rounds_hd64(split):
+    _sampled_case(2, 16, 4, 3000, 3000, 64, "f16", 23, split=split)
+
+
+
+# --------------------------------------------------------- stream-K specifics
+
+def test_streamk_single_long_row_split_over_many_ctas():
+    """One query tile pair over 8192 keys: its 64 KV steps are cut across
+    every SM and merged back by the CTA holding KV tile 0."""
+    for causal in (True, False):
+        _full_case(1, 1, 1, 200, 8192, 128, causal, "f16", seed=31, split=True)
+        _full_case(1, 2, 2, 128, 8192, 64, causal, "bf16", seed=32, split=True)
+
+
+def test_streamk_workspace_reused_across_shapes():
+    """The same workspace serves consecutive calls with different shapes (and
+    so different splits); flags of an earlier call must never satisfy a later one."""
+    cases = [(1, 4, 2, 300, 5000), (1, 1, 1, 64, 9000), (2, 8, 8, 700, 700), (1, 4, 2, 300, 5000)]
+    for n, (B, Hq, Hkv, Sq, Skv) in enumerate(cases):
+        _full_case(B, Hq, Hkv, Sq, Skv, 128, True, "f16", seed=40 + n, split=True)
+
+
+def test_streamk_is_bitwise_repeatable_and_matches_oneshot_closely():
+    fa = _fa()
+    w, (q, k, v) = _inputs(1, 4, 2, 640, 6000, 128, "bf16", 41)
+    dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
+    a = fa.attention(dq, dk, dv, causal=True, scale=w.scale, split=True).clone()
+    for _ in range(4):
+        assert torch.equal(a, fa.attention(dq, dk, dv, causal=True, scale=w.scale, split=True))
+    b = fa.attention(dq, dk, dv, causal=True, scale=w.scale, split=False)
+    assert (a.float() - b.float()).abs().max().item() < 2e-2
+
+
+def test_streamk_workspace_errors():
+    fa = _fa()
+    q = torch.randn((1, 8, 4, 128), device="cuda").half()
+    k = torch.randn((1, 8, 2, 128), device="cuda").half()
+    o = torch.empty_like(q)
+    ws = fa.workspace_for(q.device, 128)
+    assert fa.fa_prefill_ws(q, k, k, o, 1, 4, 2, 8, 8, 128, 1, 0.1, ws, ws.numel() - 1) == 1
+    assert fa.fa_prefill_ws(q, k, k, o, 1, 4, 2, 8, 8, 128, 1, 0.1, ws.data_ptr() + 128, ws.numel() - 256) == 3
+    assert fa.fa_prefill_ws(q, k, k, o, 1, 4, 2, 8, 8, 128, 1, 0.1, ws, ws.numel()) == 0
