@@ -20,7 +20,7 @@ _lib = None
 FA_OK = 0
 STATUS_NAMES = {
     0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_ALIGNMENT",
-    4: "FA_ERR_SMEM", 5: "FA_ERR_LAUNCH", 6: "FA_ERR_DEVICE",
+    4: "FA_ERR_SMEM", 5: "FA_ERR_LAUNCH", 6: "FA_ERR_DEVICE", 7: "FA_ERR_SCRATCH",
 }
 
 # (name, restype, argtypes) of every symbol include/fa_prefill.h declares
@@ -33,6 +33,7 @@ _SIG = {
     "fa_prefill_ws_bf16": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, ctypes.c_size_t,
                                 _P]),
     "fa_workspace_bytes": (ctypes.c_size_t, [_I]),
+    "fa_prefill_ws_static": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _I, _P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_smem_bytes": (ctypes.c_uint, [_I]),
     "fa_debug_status": (_I, []),
@@ -123,6 +124,15 @@ def fa_prefill_ws_bf16(q, k, v, o, B, Hq, Hkv, Sq, Skv, hd, causal, scale, works
     return int(load().fa_prefill_ws_bf16(_ptr(q), _ptr(k), _ptr(v), _ptr(o), int(B), int(Hq), int(Hkv),
                                          int(Sq), int(Skv), int(hd), int(causal), float(scale), _ptr(workspace),
                                          int(workspace_bytes), _stream(stream)))
+
+
+def fa_prefill_ws_static(q, k, v, o, B, Hq, Hkv, Sq, Skv, hd, causal, scale, bf16, stream=None) -> int:
+    """Split-KV entry point with the library's static scratch: the C function's
+    arguments (``bf16`` 0 for f16, 1 for bfloat16).  Allocates nothing: for
+    callers that cannot allocate device memory at call time.  Returns the status."""
+    return int(load().fa_prefill_ws_static(_ptr(q), _ptr(k), _ptr(v), _ptr(o), int(B), int(Hq), int(Hkv),
+                                           int(Sq), int(Skv), int(hd), int(causal), float(scale), int(bf16),
+                                           _stream(stream)))
 
 
 def workspace_bytes(hd: int) -> int:

@@ -1481,6 +1481,137 @@ static int run_ws(bool bf16, const void* q, const void* k, const void* v, void* 
               : launch_sk<64, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, causal, scale, ws, st, dev);
 }
 
+// ==================================== split-KV with library-owned scratch
+//
+// fa_prefill_ws_static: the split-KV kernel and schedule above, unchanged,
+// with its scratch in a file-scope device array instead of a caller
+// workspace.  It serves callers that cannot allocate device memory when they
+// call: an engine whose device memory is laid out once at start-up and may
+// not grow per request (an allocation at peak load can fail, or stall on the
+// allocator), and a C host with no device allocator of its own that holds
+// only the tensors it is given.  Nothing here allocates or frees device
+// memory.  Layout of the array (the kernel indexes every region by CTA slot):
+//   [0, 8 KB)         flags: 256 CTAs x 2 tiles x 4 warps (must start at zero)
+//   [8 KB, 520 KB)    m and l: 256 x 2 x 2 x 128 f32
+//   [520 KB, ...)     partial O: (the call's CTAs) x 2 x 128 x hd f32
+static __device__ __align__(256) unsigned char g_static_scratch[FA_STATIC_SCRATCH_BYTES];
+
+constexpr size_t STATIC_FLAG_BYTES = (size_t)SK_MAX_CTAS * 2 * 4 * 4;
+constexpr size_t STATIC_ML_BYTES = (size_t)SK_MAX_CTAS * 2 * 2 * BM * 4;
+constexpr size_t STATIC_O_OFF = STATIC_FLAG_BYTES + STATIC_ML_BYTES;
+static_assert(STATIC_FLAG_BYTES % 256 == 0 && STATIC_O_OFF % 256 == 0, "region alignment");
+static_assert(STATIC_O_OFF + (size_t)2 * BM * 128 * 4 <= FA_STATIC_SCRATCH_BYTES, "one CTA must fit");
+
+static size_t static_bytes_needed(int hd, int ctas) { return STATIC_O_OFF + (size_t)ctas * 2 * BM * hd * 4; }
+
+static std::mutex g_static_mu;
+static uint8_t* g_static_base[MAX_DEVICES];
+
+// Set-up, once per device (the first call): the array's device address, and
+// its flag words zeroed -- a flag equal to a call's sequence number means
+// "this piece is written", so no stale word may hold one.  The clear runs on
+// the caller's stream and is waited for.  Later calls read the cached address.
+static int static_scratch(int dev, cudaStream_t stream, uint8_t** base) {
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  if (g_static_base[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) {
+      (void)cudaGetLastError();
+      return FA_ERR_DEVICE;
+    }
+    if (cudaMemsetAsync(p, 0, STATIC_FLAG_BYTES, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return FA_ERR_LAUNCH;
+    }
+    g_static_base[dev] = static_cast<uint8_t*>(p);
+  }
+  *base = g_static_base[dev];
+  return FA_OK;
+}
+
+template <int HD, bool BF16>
+static int launch_sk_static(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int Sq,
+                            int Skv, int causal, float scale, uint8_t* base, cudaStream_t stream, int dev) {
+  using SL = SkLayout<HD>;
+  auto kern = fa_prefill_sk_kernel<HD, BF16>;
+  SkParams sp;
+  std::memset(&sp, 0, sizeof(sp));
+  Params& prm = sp.p;
+  prm.o = static_cast<uint16_t*>(o);
+  prm.B = B;
+  prm.Hq = Hq;
+  prm.Hkv = Hkv;
+  prm.Sq = Sq;
+  prm.Skv = Skv;
+  prm.G = Hq / Hkv;
+  prm.n_qtiles = (Sq + BM - 1) / BM;
+  prm.pair_heads = (prm.G % 2 == 0) ? 1 : 0;
+  prm.causal = causal ? 1 : 0;
+  prm.sl2 = scale * 1.4426950408889634f;
+  prm.watchdog_ns = WATCHDOG_NS;
+  SkSchedule sc;
+  get_schedule(prm, g_dev_sms[dev].load(), &sc);
+  if (static_bytes_needed(HD, sc.G) > FA_STATIC_SCRATCH_BYTES) return FA_ERR_SCRATCH;
+  std::memcpy(sp.su, sc.su, sizeof(int) * (sc.G + 1));
+  std::memcpy(sp.sj, sc.sj, sizeof(int) * (sc.G + 1));
+  sp.ws_flag = reinterpret_cast<unsigned*>(base);
+  sp.ws_ml = reinterpret_cast<float*>(base + STATIC_FLAG_BYTES);
+  sp.ws_o = reinterpret_cast<float4*>(base + STATIC_O_OFF);
+  unsigned seq = ++g_seq;
+  if (seq == 0) seq = ++g_seq;
+  sp.seq = seq;
+  const int slot = (HD == 128 ? 2 : 0) + (BF16 ? 1 : 0);
+  if (g_sk_attr_set[dev][slot].load() == 0) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SL::REQUEST) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return FA_ERR_SMEM;
+    }
+    g_sk_attr_set[dev][slot].store(1);
+  }
+  EncodeTiledFn enc = encoder();
+  if (!enc) return FA_ERR_LAUNCH;
+  CUtensorMap mq, mk, mv, mo;
+  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, HD) || !encode_bshd(&mk, enc, k, BF16, B, Skv, Hkv, HD) ||
+      !encode_bshd(&mv, enc, v, BF16, B, Skv, Hkv, HD) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, HD))
+    return FA_ERR_LAUNCH;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(static_cast<unsigned>(sc.G));
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = SL::REQUEST;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, sp) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return FA_ERR_LAUNCH;
+  }
+  return FA_OK;
+}
+
+static int run_static(bool bf16, const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
+                      int Sq, int Skv, int hd, int causal, float scale, void* stream) {
+  bool empty = false;
+  const int vs = validate(q, k, v, o, B, Hq, Hkv, Sq, Skv, hd, scale, &empty);
+  if (vs != FA_OK || empty) return vs;
+  int dev = -1;
+  const int ds = check_device(&dev);
+  if (ds != FA_OK) return ds;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* base = nullptr;
+  const int ss = static_scratch(dev, st, &base);
+  if (ss != FA_OK) return ss;
+  if (hd == 128)
+    return bf16 ? launch_sk_static<128, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, causal, scale, base, st, dev)
+                : launch_sk_static<128, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, causal, scale, base, st, dev);
+  return bf16 ? launch_sk_static<64, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, causal, scale, base, st, dev)
+              : launch_sk_static<64, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, causal, scale, base, st, dev);
+}
+
 }  // namespace fa
 
 // ================================================================== C ABI
@@ -1509,6 +1640,11 @@ extern "C" int fa_prefill_ws_bf16(const void* q, const void* k, const void* v, v
 
 extern "C" size_t fa_workspace_bytes(int hd) { return fa::ws_bytes_for(hd); }
 
+extern "C" int fa_prefill_ws_static(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
+                                    int Sq, int Skv, int hd, int causal, float scale, int bf16, void* stream) {
+  return fa::run_static(bf16 != 0, q, k, v, o, B, Hq, Hkv, Sq, Skv, hd, causal, scale, stream);
+}
+
 extern "C" const char* fa_status_string(int status) {
   switch (status) {
     case FA_OK: return "FA_OK";
@@ -1518,6 +1654,7 @@ extern "C" const char* fa_status_string(int status) {
     case FA_ERR_SMEM: return "FA_ERR_SMEM: shared-memory request does not fit the device";
     case FA_ERR_LAUNCH: return "FA_ERR_LAUNCH: TMA descriptor encode or kernel launch failed";
     case FA_ERR_DEVICE: return "FA_ERR_DEVICE: no current device or not an sm_103 GPU";
+    case FA_ERR_SCRATCH: return "FA_ERR_SCRATCH: the call needs more than the static scratch maximum (FA_STATIC_SCRATCH_BYTES)";
     default: return "unknown fa_status_t";
   }
 }

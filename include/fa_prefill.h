@@ -78,7 +78,9 @@ typedef enum {
     FA_ERR_SMEM = 4,         /* the kernel's shared-memory request does not
                                 fit the device, or setting it failed        */
     FA_ERR_LAUNCH = 5,       /* the launch (or TMA descriptor encode) failed */
-    FA_ERR_DEVICE = 6        /* no current device, or not an sm_103 GPU    */
+    FA_ERR_DEVICE = 6,       /* no current device, or not an sm_103 GPU    */
+    FA_ERR_SCRATCH = 7       /* fa_prefill_ws_static only: the call needs
+                                more than FA_STATIC_SCRATCH_BYTES of scratch */
 } fa_status_t;
 
 /*
@@ -140,6 +142,47 @@ int fa_prefill_ws_bf16(const void* q, const void* k, const void* v, void* o,
 /* Workspace bytes fa_prefill_ws needs for head dimension hd (0 if
  * unsupported); independent of the other sizes.  Host-only. */
 size_t fa_workspace_bytes(int hd);
+
+/* Size of the library's static device scratch array (one per device the
+ * library runs on): 20 MiB, under 0.01 % of a 288 GB GB300. */
+#define FA_STATIC_SCRATCH_BYTES (20u * 1024u * 1024u)
+
+/*
+ * fa_prefill_ws_static -- fa_prefill_ws with no caller workspace and no
+ * allocation.  The pages have no counterpart to this entry point (their
+ * kernel keeps no scratch); it is for callers that cannot allocate device
+ * memory when they call:
+ *   - an engine whose device memory is laid out once at start-up and may not
+ *     grow per request: an allocation under peak load can fail or stall on
+ *     the allocator, and would break the fixed layout;
+ *   - a C host with no device allocator of its own, holding only the tensors
+ *     it is given.
+ * Same split-KV kernel and schedule as fa_prefill_ws; the scratch (flags,
+ * m and l, partial O) is a file-scope device array of FA_STATIC_SCRATCH_BYTES
+ * inside the library.  Neither the call nor the library allocates or frees
+ * device memory.
+ *
+ * Arguments: the first 12 of fa_prefill, then
+ *   bf16    0: f16 Q/K/V/O (as fa_prefill); non-zero: bfloat16 (as fa_prefill_bf16)
+ *   stream  cudaStream_t to enqueue on (NULL = legacy default stream)
+ * Scratch need: 532480 + ctas * 1024 * hd bytes, ctas being the CTAs of the
+ * call's schedule (at most the SM count, and at most 256).  A call that needs
+ * more than FA_STATIC_SCRATCH_BYTES returns FA_ERR_SCRATCH and launches
+ * nothing; on a 152-SM GB300 every call fits (at most 20455424 bytes, hd 128).
+ * Set-up: the first call on each device looks up the array's address
+ * (cudaGetSymbolAddress) and zeroes its flag words, the part that must start
+ * at zero, on `stream`, and waits for that; make this first call before any
+ * stream capture begins.  Later calls only launch the kernel.
+ * Concurrency: every call on a device uses the same array, so calls that
+ * overlap on the GPU (issued on different streams, or from several host
+ * threads, without ordering between them) race and corrupt each other's
+ * output.  Issue them in order, e.g. on one stream.
+ * Errors: those of fa_prefill; FA_ERR_SCRATCH as above; FA_ERR_DEVICE or
+ * FA_ERR_LAUNCH if the set-up fails (it is retried by the next call).
+ */
+int fa_prefill_ws_static(const void* q, const void* k, const void* v, void* o,
+                         int B, int Hq, int Hkv, int Sq, int Skv, int hd,
+                         int causal, float scale, int bf16, void* stream);
 
 /* A static, human-readable name for a status code (never NULL). */
 const char* fa_status_string(int status);

@@ -111,3 +111,21 @@ def test_workspace_size_and_errors_without_a_device(fa):
         assert f(*args, 5 * A, ws - 1, 0) == 1        # too small
         assert f(A, 2 * A, 3 * A, 4 * A, 0, 4, 2, 8, 8, 128, 1, 0.1, 0, 0, 0) == 0  # empty problem: no-op
         assert f(A, 2 * A, 3 * A, 4 * A, 1, 4, 2, 8, 8, 96, 1, 0.1, 5 * A, ws, 0) == 2
+
+
+def test_static_scratch_entry_point_errors_without_a_device(fa):
+    """fa_prefill_ws_static checks its arguments like fa_prefill before any
+    device call (and before its one-time set-up)."""
+    f = fa.fa_prefill_ws_static
+    for bf16 in (0, 1):
+        args = dict(q=A, k=2 * A, v=3 * A, o=4 * A, B=1, Hq=4, Hkv=2, Sq=8, Skv=8, hd=128, causal=1, scale=0.1)
+
+        def call(**kw):
+            a = dict(args, **kw)
+            return f(a["q"], a["k"], a["v"], a["o"], a["B"], a["Hq"], a["Hkv"], a["Sq"], a["Skv"], a["hd"],
+                     a["causal"], a["scale"], bf16, 0)
+
+        assert call(q=0) == 1 and call(Hkv=3) == 1 and call(scale=0.0) == 1
+        assert call(hd=96) == 2 and call(q=A + 8) == 3
+        assert call(B=0) == 0 and call(Sq=0, q=0, o=0) == 0
+    assert fa.status_string(7).startswith("FA_ERR_SCRATCH")
