@@ -47,6 +47,8 @@ def parse_args(argv=None):
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--path", choices=["auto", "oneshot", "split"], default="auto",
+                    help="kernel: the library's advice for the shape (auto), one-shot, or split-KV")
     return ap.parse_args(argv)
 
 
@@ -289,11 +291,19 @@ def run_ours(args):
     for c in range(ncopy):
         copies.append((q.to(dev), k.to(dev), v.to(dev), torch.empty_like(q, device=dev)))
     stream = torch.cuda.current_stream(dev)
-    fn = fa.fa_prefill_bf16 if w.dtype == "bf16" else fa.fa_prefill
+    split = (args.path == "split" or
+             (args.path == "auto" and fa.split_kv_advised(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.causal)))
+    if split:
+        fn = fa.fa_prefill_ws_bf16 if w.dtype == "bf16" else fa.fa_prefill_ws
+        ws = torch.zeros(fa.workspace_bytes(w.hd), dtype=torch.uint8, device=dev)  # zero-filled once
+        extra = (ws, ws.numel())
+    else:
+        fn = fa.fa_prefill_bf16 if w.dtype == "bf16" else fa.fa_prefill
+        extra = ()
 
     def step(i):
         dq, dk, dv, do = copies[i % ncopy]
-        st = fn(dq, dk, dv, do, w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.hd, int(w.causal), w.scale, stream)
+        st = fn(dq, dk, dv, do, w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.hd, int(w.causal), w.scale, *extra, stream)
         if st != 0:
             raise fa.FaError(st, fn.__name__)
 
@@ -337,7 +347,7 @@ def run_ours(args):
             dq.copy_(hq_, non_blocking=True)
             dk.copy_(hk_, non_blocking=True)
             dv.copy_(hv_, non_blocking=True)
-            fa.attention(dq, dk, dv, causal=w.causal, scale=w.scale, out=do)
+            fa.attention(dq, dk, dv, causal=w.causal, scale=w.scale, out=do, split=split)
             ho.copy_(do, non_blocking=True)
 
         for _ in range(3):
@@ -367,7 +377,7 @@ def run_ours(args):
         return 0
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     achieved = flops / (ms_step * 1e-3) / 1e12
-    traffic = recorded_traffic(w.name)
+    traffic = recorded_traffic(w.name + (":split" if split else ""))
     line = {
         "metric": "causal prefill attention TFLOPS (ms/call, % of dense peak)",
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -377,7 +387,8 @@ def run_ours(args):
                    "hd": w.hd, "causal": w.causal, "scale": w.scale,
                    "flops_per_call": flops, "flop_convention": "4*hd*visible (query,key) pairs",
                    "l2": f"inputs rotated over {ncopy} resident copies ({ncopy * io / 1e6:.0f} MB > L2)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "kernel": "fa_prefill_sk_kernel (split-KV)" if split else "fa_prefill_kernel (one-shot)"},
         "pct_of_peak": 100.0 * achieved / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,

@@ -9,8 +9,8 @@ in ``include/fa_prefill.h``; this package is its Python binding.
 from ._build import LIB_PATH, build
 from ._lib import (FA_OK, FaError, attention, debug_status, debug_status_clear, fa_prefill,
                    fa_prefill_bf16, fa_prefill_ws, fa_prefill_ws_bf16, fa_prefill_ws_static, load, smem_bytes,
-                   status_string, workspace_bytes, workspace_for)
+                   split_kv_advised, status_string, workspace_bytes, workspace_for)
 
 __all__ = ["attention", "fa_prefill", "fa_prefill_bf16", "fa_prefill_ws", "fa_prefill_ws_bf16",
-           "fa_prefill_ws_static", "workspace_bytes", "workspace_for", "status_string", "smem_bytes",
+           "fa_prefill_ws_static", "split_kv_advised", "workspace_bytes", "workspace_for", "status_string", "smem_bytes",
            "debug_status", "debug_status_clear", "FaError", "FA_OK", "build", "load", "LIB_PATH"]

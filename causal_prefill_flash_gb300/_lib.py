@@ -33,6 +33,7 @@ _SIG = {
     "fa_prefill_ws_bf16": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, ctypes.c_size_t,
                                 _P]),
     "fa_workspace_bytes": (ctypes.c_size_t, [_I]),
+    "fa_split_kv_advised": (_I, [_I, _I, _I, _I, _I, _I]),
     "fa_prefill_ws_static": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _I, _P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_smem_bytes": (ctypes.c_uint, [_I]),
@@ -135,6 +136,15 @@ def fa_prefill_ws_static(q, k, v, o, B, Hq, Hkv, Sq, Skv, hd, causal, scale, bf1
                                            _stream(stream)))
 
 
+def split_kv_advised(B, Hq, Hkv, Sq, Skv, causal=True) -> bool:
+    """The library's advice for this shape on the current device: True when the
+    split-KV kernel is expected to beat the one-shot kernel."""
+    st = int(load().fa_split_kv_advised(int(B), int(Hq), int(Hkv), int(Sq), int(Skv), int(bool(causal))))
+    if st < 0:
+        raise FaError(-st, "fa_split_kv_advised")
+    return st == 1
+
+
 def workspace_bytes(hd: int) -> int:
     return int(load().fa_workspace_bytes(int(hd)))
 
@@ -155,14 +165,15 @@ def workspace_for(device, hd: int, stream=None):
 
 
 def attention(q, k, v, causal: bool = True, scale: float | None = None, out=None, stream=None,
-              split: bool = False):
+              split: bool | None = None):
     """O = softmax(scale Q K^T + causal mask) V for BSHD CUDA tensors.
 
     q: [B, Sq, Hq, hd], k/v: [B, Skv, Hkv, hd], all float16 or all bfloat16,
     contiguous, on the current CUDA device.  Returns O with q's shape and dtype
     (written into ``out`` when given).  ``split=True`` uses the load-balanced
-    stream-K kernel with a cached workspace.  Raises FaError on any library
-    error.
+    stream-K (split-KV) kernel with a cached workspace, ``split=False`` the
+    one-shot kernel, ``split=None`` whichever the library advises for the
+    shape (``split_kv_advised``).  Raises FaError on any library error.
     """
     import torch
     if not (q.is_cuda and k.is_cuda and v.is_cuda):
@@ -183,6 +194,8 @@ def attention(q, k, v, causal: bool = True, scale: float | None = None, out=None
         out = torch.empty_like(q)
     elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
         raise ValueError("out must be a contiguous CUDA tensor like q")
+    if split is None:
+        split = split_kv_advised(B, Hq, Hkv, Sq, Skv, causal)
     if split:
         fn = fa_prefill_ws_bf16 if q.dtype == torch.bfloat16 else fa_prefill_ws
         ws = workspace_for(q.device, hd, stream)

@@ -1640,6 +1640,19 @@ extern "C" int fa_prefill_ws_bf16(const void* q, const void* k, const void* v, v
 
 extern "C" size_t fa_workspace_bytes(int hd) { return fa::ws_bytes_for(hd); }
 
+extern "C" int fa_split_kv_advised(int B, int Hq, int Hkv, int Sq, int Skv, int causal) {
+  (void)causal;  // the longest query tile walks all Skv keys either way (bottom-right alignment)
+  if (B < 0 || Sq < 0 || Skv < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return -FA_ERR_INVALID_ARG;
+  if (B == 0 || Sq == 0 || Skv == 0) return 0;
+  int dev = -1;
+  const int ds = fa::check_device(&dev);
+  if (ds != FA_OK) return -ds;
+  const long long units = fa::grid_size(B, Hq, Hkv, Sq);
+  const long long longest = (Skv + fa::BN - 1) / fa::BN;
+  const long long sms = fa::g_dev_sms[dev].load();
+  return (2 * units <= sms && longest >= 8) ? 1 : 0;
+}
+
 extern "C" int fa_prefill_ws_static(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
                                     int Sq, int Skv, int hd, int causal, float scale, int bf16, void* stream) {
   return fa::run_static(bf16 != 0, q, k, v, o, B, Hq, Hkv, Sq, Skv, hd, causal, scale, stream);

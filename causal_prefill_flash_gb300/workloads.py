@@ -86,6 +86,9 @@ WORKLOADS = [
              note="chunked prefill: 512 new rows over 7680 cached + 512 new keys, f16"),
     Workload("chunked_kv8192_hd64", 4, 32, 8, 512, 8192, 64, seed=1239,
              note="chunked prefill at hd=64, f16"),
+    Workload("longctx_chunk128_kv32768", 1, 32, 8, 128, 32768, 128, seed=1240,
+             note="a 128-row chunk over a 32640-token cached context: 16 query-tile pairs, "
+                  "each 256 KV tiles long (an underfilled grid), f16"),
 ]
 BY_NAME = {w.name: w for w in WORKLOADS}
 

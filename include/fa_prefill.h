@@ -143,6 +143,21 @@ int fa_prefill_ws_bf16(const void* q, const void* k, const void* v, void* o,
  * unsupported); independent of the other sizes.  Host-only. */
 size_t fa_workspace_bytes(int hd);
 
+/*
+ * fa_split_kv_advised -- host-only advice on which kernel to call for a shape
+ * on the current device: 1 if fa_prefill_ws (split-KV) is expected to be
+ * faster than fa_prefill, 0 if not, a negative fa_status_t on error (-1 bad
+ * sizes, -6 no usable device).  The rule is the pages' split-K rule for an
+ * underfilled part, applied to the KV dimension (page "mate: Marlin-class
+ * W4A16 GEMM for mp_31 (SQMMA int4 x fp16) - #6", section "Split-K: the
+ * decode occupancy lever": split when the tiles cannot cover the part, but
+ * only when each piece keeps enough work to pay for the merge): split when
+ * the one-shot grid (query-tile pairs) covers at most half of the SMs and the
+ * longest query tile walks at least 8 KV tiles.  Queries the device's SM
+ * count once (cached); launches nothing.
+ */
+int fa_split_kv_advised(int B, int Hq, int Hkv, int Sq, int Skv, int causal);
+
 /* Size of the library's static device scratch array (one per device the
  * library runs on): 20 MiB, under 0.01 % of a 288 GB GB300. */
 #define FA_STATIC_SCRATCH_BYTES (20u * 1024u * 1024u)

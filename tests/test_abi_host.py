@@ -129,3 +129,11 @@ def test_static_scratch_entry_point_errors_without_a_device(fa):
         assert call(hd=96) == 2 and call(q=A + 8) == 3
         assert call(B=0) == 0 and call(Sq=0, q=0, o=0) == 0
     assert fa.status_string(7).startswith("FA_ERR_SCRATCH")
+
+
+def test_split_advice_rejects_bad_sizes_without_a_device(fa):
+    f = fa._lib.load().fa_split_kv_advised
+    assert f(1, 3, 2, 8, 8, 1) == -1      # Hq % Hkv != 0
+    assert f(-1, 4, 2, 8, 8, 1) == -1
+    assert f(0, 4, 2, 8, 8, 1) == 0       # nothing to compute: no advice needed, no device touched
+    assert f(1, 4, 2, 8, 0, 1) == 0

@@ -6,7 +6,7 @@ from causal_prefill_flash_gb300 import workloads as W
 
 def test_table_shapes_and_counts():
     names = [w.name for w in W.WORKLOADS]
-    assert len(names) == len(set(names)) == 6
+    assert len(names) == len(set(names)) == 7
     c = {w.name: w for w in W.WORKLOADS}
     # algorithmic FLOPs = 4 * hd * visible (row, key) pairs
     assert c["single_head_s256"].flops() == 4 * 128 * (256 * 257 // 2)
@@ -17,6 +17,8 @@ def test_table_shapes_and_counts():
     per_head = sum(7681 + i for i in range(512))
     assert c["chunked_kv8192_hd128"].flops() == 4 * 128 * 4 * 32 * per_head
     assert c["chunked_kv8192_hd64"].flops() == 4 * 64 * 4 * 32 * per_head
+    # long context: row i of the 128-row chunk sees 32640 + i + 1 keys
+    assert c["longctx_chunk128_kv32768"].flops() == 4 * 128 * 32 * sum(32641 + i for i in range(128))
 
 
 def test_inputs_are_seeded_and_typed():
