@@ -69,6 +69,12 @@ def _load():
             lib.oracle_probs_row.restype = i32
             lib.oracle_plant_mistake.argtypes = [i32]
             lib.oracle_plant_mistake.restype = i32
+            lib.oracle_round_f16.argtypes = [ctypes.c_float]
+            lib.oracle_round_f16.restype = ctypes.c_uint16
+            lib.oracle_round_bf16.argtypes = [ctypes.c_float]
+            lib.oracle_round_bf16.restype = ctypes.c_uint16
+            lib.oracle_kv_append.argtypes = ([ctypes.c_void_p] * 5 + [i32] * 6)
+            lib.oracle_kv_append.restype = ctypes.c_longlong
             _lib = lib
     return _lib
 
@@ -78,6 +84,7 @@ def _load():
 PLANTED_MISTAKES = {
     "none": 0, "no_scale": 1, "top_left": 2, "mask_off_by_one": 3, "gqa_modulo": 4,
     "no_normalise": 5, "v_reversed": 6, "no_max_subtract": 7, "exp2": 8, "masked_row_nan": 9,
+    "round_truncate": 10, "round_ties_away": 11, "append_at_t": 12,
 }
 
 
@@ -163,3 +170,34 @@ def probs_row(q, k, b: int, hq: int, i: int, causal: bool = True,
     if rc != 0:
         raise ValueError(f"oracle_probs_row failed with status {rc}")
     return p
+
+
+def round16_bits(x, bf16: bool) -> np.ndarray:
+    """IEEE round-to-nearest-even of float32 values into binary16 (bf16=False)
+    or bfloat16 (bf16=True); returns the 16-bit patterns as uint16."""
+    lib = _load()
+    f = lib.oracle_round_bf16 if bf16 else lib.oracle_round_f16
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float32)).ravel()
+    out = np.empty(a.shape, dtype=np.uint16)
+    for i, v in enumerate(a.tolist()):
+        out[i] = f(v)
+    return out.reshape(np.shape(x))
+
+
+def kv_append(k_new, v_new, positions, k_cache_bits, v_cache_bits, bf16: bool):
+    """The K/V-cache append on numpy arrays: k_new, v_new float32 [B][T][Hkv][hd];
+    positions int32 [B][T]; caches uint16 bit patterns [B][cap][Hkv][hd],
+    updated in place.  Returns the number of tokens skipped (position out of range)."""
+    kn = np.ascontiguousarray(k_new, dtype=np.float32)
+    vn = np.ascontiguousarray(v_new, dtype=np.float32)
+    ps = np.ascontiguousarray(positions, dtype=np.int32)
+    for c in (k_cache_bits, v_cache_bits):
+        if c.dtype != np.uint16 or not c.flags.c_contiguous:
+            raise ValueError("caches must be contiguous uint16 arrays")
+    B, T, Hkv, hd = kn.shape
+    cap = k_cache_bits.shape[1]
+    n = _load().oracle_kv_append(kn.ctypes.data, vn.ctypes.data, ps.ctypes.data, k_cache_bits.ctypes.data,
+                                 v_cache_bits.ctypes.data, B, T, Hkv, hd, cap, int(bool(bf16)))
+    if n < 0:
+        raise ValueError("bad arguments")
+    return int(n)

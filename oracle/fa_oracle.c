@@ -61,7 +61,10 @@ enum {
     PLANT_NO_MAX_SUBTRACT = 7, /* exp(s_j) without subtracting the max      */
     PLANT_EXP2 = 8,            /* base-2 exponential instead of e           */
     PLANT_MASKED_ROW_NAN = 9,  /* no guard for rows that see no key         */
-    PLANT_COUNT = 10
+    PLANT_ROUND_TRUNCATE = 10, /* cache append rounds toward zero           */
+    PLANT_ROUND_TIES_AWAY = 11,/* cache append breaks ties away from zero   */
+    PLANT_APPEND_AT_T = 12,    /* cache append writes row t, not positions[t] */
+    PLANT_COUNT = 13
 };
 static int g_plant = PLANT_NONE;
 
@@ -268,4 +271,95 @@ int oracle_probs_row(const double *q, const double *k,
     double m = score_row(&s, b, hq, i, p);
     softmax_row(p, Skv, m);
     return ORACLE_OK;
+}
+
+
+/* ------------------------------------------------------------------------
+ * K/V-cache append (the step before a chunked prefill's attention: the pages'
+ * store_kv kernel, minfer "11 · P5 — prefill gap session: TM=128 big tiles +
+ * FA rewrite", section 3.2: an f32 token row is written as 16-bit values at
+ * cache row positions[t]):
+ *
+ *   cache[b][positions[b][t]][h][d] = round16(new[b][t][h][d])   for K and V
+ *
+ * round16 is IEEE 754 round-to-nearest, ties to even, into binary16 or
+ * bfloat16 (8 significant bits, binary32's exponent range).  Written from the
+ * definition: |f| is exact in double; it is divided by the spacing (ulp) of
+ * the target grid in its binade -- a power of two, so exactly -- rounded to an
+ * integer with rint() (ties to even in the default rounding mode) and
+ * multiplied back; results above the largest finite value become infinity;
+ * NaN stays NaN (quiet); the sign is kept, zeros included.
+ */
+
+/* mbits: stored significand bits; ebits: exponent bits. */
+static uint16_t round16(float f, int mbits, int ebits)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    const uint16_t sign = (uint16_t)((u >> 31) << 15);
+    const int bias = (1 << (ebits - 1)) - 1;
+    const int emin = 1 - bias, emax = bias;
+    const uint16_t exp_ones = (uint16_t)(((1u << ebits) - 1) << mbits);
+    if (isnan(f)) return (uint16_t)(sign | exp_ones | (1u << (mbits - 1)));
+    if (isinf(f)) return (uint16_t)(sign | exp_ones);
+    const double x = fabs((double)f);
+    if (x == 0.0) return sign;
+    int e;
+    frexp(x, &e);               /* x in [2^(e-1), 2^e) */
+    int E = e - 1;              /* binade exponent */
+    if (E < emin) E = emin;     /* the subnormal range shares the smallest binade's spacing */
+    const double ulp = ldexp(1.0, E - mbits);
+    const double t = x / ulp;   /* exact */
+    double n;
+    if (g_plant == PLANT_ROUND_TRUNCATE) {
+        n = floor(t);
+    } else if (g_plant == PLANT_ROUND_TIES_AWAY) {
+        n = floor(t + 0.5);
+    } else {
+        n = rint(t);            /* nearest, ties to even */
+    }
+    const double r = n * ulp;
+    const double max_finite = ldexp(2.0 - ldexp(1.0, -mbits), emax);
+    if (r > max_finite) return (uint16_t)(sign | exp_ones);
+    if (r == 0.0) return sign;
+    if (r < ldexp(1.0, emin))   /* subnormal: exponent field 0 */
+        return (uint16_t)(sign | (uint16_t)(r / ldexp(1.0, emin - mbits)));
+    int e2;
+    frexp(r, &e2);
+    const int E2 = e2 - 1;
+    const uint16_t mant = (uint16_t)(r / ldexp(1.0, E2 - mbits) - (double)(1u << mbits));
+    return (uint16_t)(sign | (uint16_t)((E2 + bias) << mbits) | mant);
+}
+
+uint16_t oracle_round_f16(float f) { return round16(f, 10, 5); }
+uint16_t oracle_round_bf16(float f) { return round16(f, 7, 8); }
+
+/* new: [B][T][Hkv][hd] f32; positions: [B][T]; cache: [B][cap][Hkv][hd]
+ * 16-bit patterns.  Tokens whose position is outside [0, cap) are skipped;
+ * returns the number skipped (>= 0), or -ORACLE_BAD_ARG. */
+long long oracle_kv_append(const float *k_new, const float *v_new, const int32_t *positions,
+                           uint16_t *k_cache, uint16_t *v_cache,
+                           int B, int T, int Hkv, int hd, int cap, int bf16)
+{
+    if (B < 0 || T < 0 || Hkv < 1 || hd < 1 || cap < 1) return -ORACLE_BAD_ARG;
+    const long long row = (long long)Hkv * hd;
+    long long skipped = 0;
+    for (int b = 0; b < B; ++b) {
+        for (int t = 0; t < T; ++t) {
+            const int pos = (g_plant == PLANT_APPEND_AT_T) ? t : positions[(long long)b * T + t];
+            if (pos < 0 || pos >= cap) {
+                ++skipped;
+                continue;
+            }
+            const float *ks = k_new + ((long long)b * T + t) * row;
+            const float *vs = v_new + ((long long)b * T + t) * row;
+            uint16_t *kd = k_cache + ((long long)b * cap + pos) * row;
+            uint16_t *vd = v_cache + ((long long)b * cap + pos) * row;
+            for (long long x = 0; x < row; ++x) {
+                kd[x] = bf16 ? oracle_round_bf16(ks[x]) : oracle_round_f16(ks[x]);
+                vd[x] = bf16 ? oracle_round_bf16(vs[x]) : oracle_round_f16(vs[x]);
+            }
+        }
+    }
+    return skipped;
 }

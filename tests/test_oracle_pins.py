@@ -338,6 +338,88 @@ def test_bad_arguments_are_rejected():
 
 
 # --------------------------------------------------------------------------
+# K/V-cache append: IEEE round-to-nearest-even into 16 bits, scattered to
+# positions.  The roundings reduce to library conversions (numpy's float32 ->
+# float16 and torch's float32 -> bfloat16, both round to nearest even), and
+# hand-picked ties fix the tie rule on their own.
+# --------------------------------------------------------------------------
+
+def _round_probe_values():
+    rng = np.random.default_rng(7)
+    bits = rng.integers(0, 2 ** 32, size=60000, dtype=np.uint64).astype(np.uint32)
+    rand = bits.view(np.float32)
+    rand = rand[~np.isnan(rand)]
+    # values around every f16 and bf16 binade, including the subnormal ranges
+    scaled = (rng.standard_normal(40000) * np.exp2(rng.integers(-30, 18, size=40000))).astype(np.float32)
+    tiny = (rng.standard_normal(20000) * np.exp2(rng.integers(-140, -120, size=20000))).astype(np.float32)
+    special = np.array([0.0, -0.0, np.inf, -np.inf, 1.0, -1.0, 65504.0, 65519.996, 65520.0, 65536.0,
+                        2.0 ** -24, 2.0 ** -25, 1.5 * 2.0 ** -24, 2.0 ** -14, 2.0 ** -15,
+                        1 + 2.0 ** -11, 1 + 3 * 2.0 ** -11, 1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8,
+                        np.finfo(np.float32).max, np.finfo(np.float32).tiny, 2.0 ** -149, 2.0 ** -133,
+                        2.0 ** -134, 3 * 2.0 ** -135], dtype=np.float32)
+    return np.concatenate([rand, scaled, tiny, special, -special])
+
+
+def test_round_f16_matches_ieee_conversion():
+    x = _round_probe_values()
+    with np.errstate(over="ignore"):
+        want = x.astype(np.float16).view(np.uint16)
+    got = oracle.round16_bits(x, bf16=False)
+    assert np.array_equal(got, want)
+
+
+def test_round_bf16_matches_ieee_conversion():
+    x = _round_probe_values()
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.round16_bits(x, bf16=True)
+    assert np.array_equal(got, want)
+
+
+def test_round_ties_go_to_even():
+    """Halfway cases, by hand: 1 + 2^-11 lies halfway between 1 and the next
+    f16 (1 + 2^-10) and rounds to 1 (even); 1 + 3 2^-11 rounds up to 1 + 2^-9;
+    2^-25 (half the smallest f16 subnormal) rounds to 0; 65520 rounds to
+    2^16, past the largest f16, so to infinity; likewise for bf16 at 2^-8."""
+    f16 = lambda v: int(oracle.round16_bits(np.float32(v), bf16=False))
+    bf = lambda v: int(oracle.round16_bits(np.float32(v), bf16=True))
+    assert f16(1 + 2.0 ** -11) == 0x3C00 and f16(1 + 3 * 2.0 ** -11) == 0x3C02
+    assert f16(2.0 ** -25) == 0x0000 and f16(1.5 * 2.0 ** -24) == 0x0002 and f16(65520.0) == 0x7C00
+    assert bf(1 + 2.0 ** -8) == 0x3F80 and bf(1 + 3 * 2.0 ** -8) == 0x3F82
+    assert f16(-0.0) == 0x8000 and bf(float("-inf")) == 0xFF80
+    assert f16(float("nan")) & 0x7C00 == 0x7C00 and f16(float("nan")) & 0x03FF
+
+
+def test_kv_append_scatters_rounded_rows_to_positions():
+    """Brute force on a tiny cache: every token's K and V row lands, rounded,
+    at its position; untouched rows keep their contents; out-of-range
+    positions are skipped and counted."""
+    rng = np.random.default_rng(11)
+    B, T, Hkv, hd, cap = 2, 5, 2, 8, 16
+    k_new = (rng.standard_normal((B, T, Hkv, hd)) * 3).astype(np.float32)
+    v_new = (rng.standard_normal((B, T, Hkv, hd)) * 3).astype(np.float32)
+    pos = np.stack([rng.permutation(cap)[:T] for _ in range(B)]).astype(np.int32)
+    pos[1, 2] = cap      # out of range: skipped
+    pos[0, 4] = -1       # out of range: skipped
+    for bf16 in (False, True):
+        kc = np.full((B, cap, Hkv, hd), 0xABCD, dtype=np.uint16)
+        vc = np.full((B, cap, Hkv, hd), 0x1234, dtype=np.uint16)
+        skipped = oracle.kv_append(k_new, v_new, pos, kc, vc, bf16=bf16)
+        assert skipped == 2
+        if bf16:
+            cvt = lambda a: torch.from_numpy(a).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        else:
+            cvt = lambda a: a.astype(np.float16).view(np.uint16)
+        wk = np.full_like(kc, 0xABCD)
+        wv = np.full_like(vc, 0x1234)
+        for b in range(B):
+            for t in range(T):
+                if 0 <= pos[b, t] < cap:
+                    wk[b, pos[b, t]] = cvt(k_new[b, t])
+                    wv[b, pos[b, t]] = cvt(v_new[b, t])
+        assert np.array_equal(kc, wk) and np.array_equal(vc, wv)
+
+
+# --------------------------------------------------------------------------
 # planted mistakes: each wrong variant of the oracle fails at least one pin
 # --------------------------------------------------------------------------
 
@@ -359,6 +441,10 @@ def _pin_battery():
         ("masked_rows", test_fully_masked_rows_are_zero),
         ("scale", test_scale_applies_to_scores),
         ("large_scores", test_large_scores_are_stable),
+        ("round_f16", test_round_f16_matches_ieee_conversion),
+        ("round_bf16", test_round_bf16_matches_ieee_conversion),
+        ("round_ties", test_round_ties_go_to_even),
+        ("kv_append", test_kv_append_scatters_rounded_rows_to_positions),
     ]
 
 
