@@ -47,6 +47,8 @@ def parse_args(argv=None):
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--op", choices=["attention", "kv_append"], default="attention",
+                    help="attention (the default line) or the K/V-cache append of the workload's whole K/V")
     ap.add_argument("--path", choices=["auto", "oneshot", "split"], default="auto",
                     help="kernel: the library's advice for the shape (auto), one-shot, or split-KV")
     return ap.parse_args(argv)
@@ -408,10 +410,78 @@ def run_ours(args):
     return 0
 
 
+def run_append(args):
+    """The K/V-cache append on one GPU: the workload's whole K and V (Skv tokens
+    per sequence, f32) rounded into 16-bit caches at positions 0..Skv-1.  HBM
+    bound: reports GB/s of algorithmic traffic (f32 read, 16-bit written,
+    positions read) against the measured copy bandwidth."""
+    import torch
+    import causal_prefill_flash_gb300 as fa
+    from causal_prefill_flash_gb300 import workloads as W
+
+    rank, world, local = dist_env()
+    if world > 1 and rank != 0:
+        return 0
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = W.get(args.workload)
+    B, T, Hkv, hd = w.B, w.Skv, w.Hkv, w.hd
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed)
+    k_new = torch.randn((B, T, Hkv, hd), generator=g, dtype=torch.float32)
+    v_new = torch.randn((B, T, Hkv, hd), generator=g, dtype=torch.float32)
+    pos = torch.arange(T, dtype=torch.int32).repeat(B, 1).contiguous()
+    dt = w.torch_dtype
+    n = B * T * Hkv * hd
+    step_bytes = 2 * n * 4 + 2 * n * 2 + B * T * 4
+    ncopy = max(2, math.ceil(3 * L2_BYTES / step_bytes))
+    copies = [(k_new.to(dev), v_new.to(dev), pos.to(dev), torch.empty((B, T, Hkv, hd), dtype=dt, device=dev),
+               torch.empty((B, T, Hkv, hd), dtype=dt, device=dev)) for _ in range(ncopy)]
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        kn, vn, ps, kc, vc = copies[i % ncopy]
+        st = fa.fa_kv_append(kn, vn, ps, kc, vc, B, T, Hkv, hd, T, int(dt == torch.bfloat16), stream)
+        if st != 0:
+            raise fa.FaError(st, "fa_kv_append")
+
+    peaks, peak_src = load_peaks()
+    with ClockSampler(local) as clocks:
+        t0 = time.time()
+        for i in range(args.warmup):
+            step(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        clocks.mark(t0, time.time())
+    ms = e0.elapsed_time(e1) / args.steps
+    gbs = step_bytes / (ms * 1e-3) / 1e9
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    line = {
+        "metric": "K/V-cache append GB/s", "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32->" + w.dtype, "data": "synthetic",
+        "config": {"workload": w.name + " K/V append", "B": B, "T": T, "Hkv": Hkv, "hd": hd,
+                   "bytes_per_step": step_bytes,
+                   "l2": f"inputs rotated over {ncopy} copies ({ncopy * step_bytes / 1e6:.0f} MB > L2)"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                     "peak_source": f"{peak_src} copy bandwidth", "traffic": None},
+        "clocks": clocks.summary(), "gpu_launches": args.steps, "watchdog_status": fa.debug_status(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.op == "kv_append":
+        return run_append(args)
     return run_ours(args)
 
 

@@ -34,6 +34,9 @@ _SIG = {
                                 _P]),
     "fa_workspace_bytes": (ctypes.c_size_t, [_I]),
     "fa_split_kv_advised": (_I, [_I, _I, _I, _I, _I, _I]),
+    "fa_prefill_kvcache": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _I, _P,
+                                ctypes.c_size_t, _P]),
+    "fa_kv_append": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "fa_prefill_ws_static": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _I, _P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_smem_bytes": (ctypes.c_uint, [_I]),
@@ -134,6 +137,78 @@ def fa_prefill_ws_static(q, k, v, o, B, Hq, Hkv, Sq, Skv, hd, causal, scale, bf1
     return int(load().fa_prefill_ws_static(_ptr(q), _ptr(k), _ptr(v), _ptr(o), int(B), int(Hq), int(Hkv),
                                            int(Sq), int(Skv), int(hd), int(causal), float(scale), int(bf16),
                                            _stream(stream)))
+
+
+def fa_prefill_kvcache(q, k_cache, v_cache, o, B, Hq, Hkv, Sq, kv_len, kv_cap, hd, causal, scale, bf16,
+                       workspace=None, workspace_bytes=0, stream=None) -> int:
+    """Attention over a K/V cache: the C function's arguments. Returns the status."""
+    return int(load().fa_prefill_kvcache(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), int(B), int(Hq),
+                                         int(Hkv), int(Sq), int(kv_len), int(kv_cap), int(hd), int(causal),
+                                         float(scale), int(bf16), _ptr(workspace), int(workspace_bytes),
+                                         _stream(stream)))
+
+
+def fa_kv_append(k_new, v_new, positions, k_cache, v_cache, B, T, Hkv, hd, kv_cap, bf16, stream=None) -> int:
+    """K/V-cache append: the C function's arguments. Returns the status."""
+    return int(load().fa_kv_append(_ptr(k_new), _ptr(v_new), _ptr(positions), _ptr(k_cache), _ptr(v_cache),
+                                   int(B), int(T), int(Hkv), int(hd), int(kv_cap), int(bf16), _stream(stream)))
+
+
+def kv_append(k_new, v_new, positions, k_cache, v_cache, stream=None):
+    """Write the f32 rows k_new, v_new [B, T, Hkv, hd] into the 16-bit caches
+    [B, kv_cap, Hkv, hd] at rows positions [B, T] (int32), rounded to the
+    caches' dtype.  All CUDA tensors, contiguous.  Raises FaError on error."""
+    import torch
+    if k_new.dtype != torch.float32 or v_new.dtype != torch.float32:
+        raise ValueError("k_new and v_new must be float32")
+    if k_cache.dtype != v_cache.dtype or k_cache.dtype not in (torch.float16, torch.bfloat16):
+        raise ValueError("caches must both be float16 or both bfloat16")
+    if positions.dtype != torch.int32:
+        raise ValueError("positions must be int32")
+    for t in (k_new, v_new, positions, k_cache, v_cache):
+        if not (t.is_cuda and t.is_contiguous()):
+            raise ValueError("all tensors must be contiguous CUDA tensors")
+    B, T, Hkv, hd = k_new.shape
+    if v_new.shape != k_new.shape or positions.shape != (B, T) or k_cache.shape != v_cache.shape \
+            or k_cache.dim() != 4 or k_cache.shape[0] != B or k_cache.shape[2:] != (Hkv, hd):
+        raise ValueError("shape mismatch")
+    st = fa_kv_append(k_new, v_new, positions, k_cache, v_cache, B, T, Hkv, hd, k_cache.shape[1],
+                      int(k_cache.dtype == torch.bfloat16), stream)
+    if st != FA_OK:
+        raise FaError(st, "fa_kv_append")
+
+
+def attention_kvcache(q, k_cache, v_cache, kv_len: int, causal: bool = True, scale: float | None = None,
+                      out=None, stream=None, split: bool | None = None):
+    """O = softmax(scale Q K^T + causal mask) V over the first kv_len rows of
+    the caches [B, kv_cap, Hkv, hd] (the query rows are the last Sq of those
+    kv_len positions).  ``split`` as in ``attention``.  Raises FaError."""
+    import torch
+    if q.dim() != 4 or k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
+        raise ValueError("q must be [B, Sq, Hq, hd] and the caches [B, kv_cap, Hkv, hd]")
+    if not (q.dtype == k_cache.dtype == v_cache.dtype) or q.dtype not in (torch.float16, torch.bfloat16):
+        raise ValueError("q and the caches must all be float16 or all bfloat16")
+    for t in (q, k_cache, v_cache):
+        if not (t.is_cuda and t.is_contiguous()):
+            raise ValueError("q and the caches must be contiguous CUDA tensors")
+    B, Sq, Hq, hd = q.shape
+    Bk, kv_cap, Hkv, hdk = k_cache.shape
+    if Bk != B or hdk != hd:
+        raise ValueError("shape mismatch")
+    if scale is None:
+        scale = 1.0 / math.sqrt(hd)
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
+        raise ValueError("out must be a contiguous CUDA tensor like q")
+    if split is None:
+        split = split_kv_advised(B, Hq, Hkv, Sq, kv_len, causal)
+    ws = workspace_for(q.device, hd, stream) if split else None
+    st = fa_prefill_kvcache(q, k_cache, v_cache, out, B, Hq, Hkv, Sq, kv_len, kv_cap, hd, int(bool(causal)),
+                            scale, int(q.dtype == torch.bfloat16), ws, ws.numel() if ws is not None else 0, stream)
+    if st != FA_OK:
+        raise FaError(st, "fa_prefill_kvcache")
+    return out
 
 
 def split_kv_advised(B, Hq, Hkv, Sq, Skv, causal=True) -> bool:

@@ -1161,9 +1161,15 @@ static EncodeTiledFn encoder() {
 }
 
 // 4-D map over a BSHD tensor: dims (hd, H, S, B), box (64, 1, 128, 1), 128-byte swizzle.
-static bool encode_bshd(CUtensorMap* m, EncodeTiledFn enc, const void* base, bool bf16, int B, int S, int H, int hd) {
-  const cuuint64_t dims[4] = {(cuuint64_t)hd, (cuuint64_t)H, (cuuint64_t)(S > 0 ? S : 1), (cuuint64_t)B};
-  const cuuint64_t strides[3] = {(cuuint64_t)hd * 2, (cuuint64_t)H * hd * 2, (cuuint64_t)(S > 0 ? S : 1) * H * hd * 2};
+// A [B][S_stride][H][hd] 16-bit tensor of which rows [0, S) of each batch are
+// described: rows from S on are out of bounds for the map, so TMA loads them
+// as zeros (S_stride = S for a contiguous BSHD tensor; a KV cache's capacity
+// otherwise).
+static bool encode_bshd(CUtensorMap* m, EncodeTiledFn enc, const void* base, bool bf16, int B, int S, int H, int hd,
+                        int S_stride) {
+  const cuuint64_t rows = (cuuint64_t)(S > 0 ? S : 1), rows_mem = (cuuint64_t)(S_stride > S ? S_stride : rows);
+  const cuuint64_t dims[4] = {(cuuint64_t)hd, (cuuint64_t)H, rows, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)hd * 2, (cuuint64_t)H * hd * 2, rows_mem * H * hd * 2};
   const cuuint32_t box[4] = {64, 1, 128, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
@@ -1227,7 +1233,7 @@ static bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 template <int HD, bool BF16>
 static int launch(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int Sq, int Skv,
-                  int causal, float scale, cudaStream_t stream, int dev) {
+                  int kv_cap, int causal, float scale, cudaStream_t stream, int dev) {
   using L = Layout<HD>;
   auto kern = fa_prefill_kernel<HD, BF16>;
   const int slot = (HD == 128 ? 2 : 0) + (BF16 ? 1 : 0);
@@ -1241,8 +1247,8 @@ static int launch(const void* q, const void* k, const void* v, void* o, int B, i
   EncodeTiledFn enc = encoder();
   if (!enc) return FA_ERR_LAUNCH;
   CUtensorMap mq, mk, mv, mo;
-  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, HD) || !encode_bshd(&mk, enc, k, BF16, B, Skv, Hkv, HD) ||
-      !encode_bshd(&mv, enc, v, BF16, B, Skv, Hkv, HD) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, HD))
+  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, HD, Sq) || !encode_bshd(&mk, enc, k, BF16, B, Skv, Hkv, HD, kv_cap) ||
+      !encode_bshd(&mv, enc, v, BF16, B, Skv, Hkv, HD, kv_cap) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, HD, Sq))
     return FA_ERR_LAUNCH;
   Params prm;
   prm.o = static_cast<uint16_t*>(o);
@@ -1304,10 +1310,10 @@ static int run(bool bf16, const void* q, const void* k, const void* v, void* o, 
   if (ds != FA_OK) return ds;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (hd == 128)
-    return bf16 ? launch<128, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, causal, scale, st, dev)
-                : launch<128, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, causal, scale, st, dev);
-  return bf16 ? launch<64, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, causal, scale, st, dev)
-              : launch<64, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, causal, scale, st, dev);
+    return bf16 ? launch<128, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev)
+                : launch<128, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev);
+  return bf16 ? launch<64, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev)
+              : launch<64, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev);
 }
 
 // ------------------------------------------------------ stream-K host side
@@ -1401,7 +1407,7 @@ static std::atomic<unsigned> g_seq{0};
 
 template <int HD, bool BF16>
 static int launch_sk(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int Sq, int Skv,
-                     int causal, float scale, void* ws, cudaStream_t stream, int dev) {
+                     int kv_cap, int causal, float scale, void* ws, cudaStream_t stream, int dev) {
   using SL = SkLayout<HD>;
   auto kern = fa_prefill_sk_kernel<HD, BF16>;
   const int slot = (HD == 128 ? 2 : 0) + (BF16 ? 1 : 0);
@@ -1415,8 +1421,8 @@ static int launch_sk(const void* q, const void* k, const void* v, void* o, int B
   EncodeTiledFn enc = encoder();
   if (!enc) return FA_ERR_LAUNCH;
   CUtensorMap mq, mk, mv, mo;
-  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, HD) || !encode_bshd(&mk, enc, k, BF16, B, Skv, Hkv, HD) ||
-      !encode_bshd(&mv, enc, v, BF16, B, Skv, Hkv, HD) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, HD))
+  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, HD, Sq) || !encode_bshd(&mk, enc, k, BF16, B, Skv, Hkv, HD, kv_cap) ||
+      !encode_bshd(&mv, enc, v, BF16, B, Skv, Hkv, HD, kv_cap) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, HD, Sq))
     return FA_ERR_LAUNCH;
   SkParams sp;
   std::memset(&sp, 0, sizeof(sp));
@@ -1462,6 +1468,44 @@ static int launch_sk(const void* q, const void* k, const void* v, void* o, int B
   return FA_OK;
 }
 
+// Attention over a K/V cache of kv_cap rows per sequence of which the first
+// kv_len are valid: the maps describe kv_len rows with a batch stride of
+// kv_cap, so rows past kv_len (stale or unwritten cache) load as zeros.
+static int run_kvcache(bool bf16, const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
+                       int Sq, int kv_len, int kv_cap, int hd, int causal, float scale, void* ws, size_t ws_bytes,
+                       void* stream) {
+  if (kv_len < 0 || kv_cap < 0 || kv_len > kv_cap) return FA_ERR_INVALID_ARG;
+  bool empty = false;
+  const int vs = validate(q, k, v, o, B, Hq, Hkv, Sq, kv_len, hd, scale, &empty);
+  if (vs != FA_OK || empty) return vs;
+  if ((long long)kv_cap > 0x7FFFFFFFLL - 256 || (unsigned long long)kv_cap * Hkv * hd * 2 >= (1ull << 40))
+    return FA_ERR_UNSUPPORTED;
+  const unsigned long long qn = (unsigned long long)B * Sq * Hq * hd;
+  const unsigned long long cn = (unsigned long long)B * kv_cap * Hkv * hd;
+  if (kv_len > 0 && (overlaps(o, qn * 2, k, cn * 2) || overlaps(o, qn * 2, v, cn * 2))) return FA_ERR_INVALID_ARG;
+  if (ws) {
+    if (reinterpret_cast<uintptr_t>(ws) & 255u) return FA_ERR_ALIGNMENT;
+    if (ws_bytes < ws_bytes_for(hd)) return FA_ERR_INVALID_ARG;
+  }
+  int dev = -1;
+  const int ds = check_device(&dev);
+  if (ds != FA_OK) return ds;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int stride = kv_len > 0 ? kv_cap : 0;  // kv_len == 0: the maps point at q (no key is loaded)
+  if (ws) {
+    if (hd == 128)
+      return bf16 ? launch_sk<128, true>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, ws, st, dev)
+                  : launch_sk<128, false>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, ws, st, dev);
+    return bf16 ? launch_sk<64, true>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, ws, st, dev)
+                : launch_sk<64, false>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, ws, st, dev);
+  }
+  if (hd == 128)
+    return bf16 ? launch<128, true>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, st, dev)
+                : launch<128, false>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, st, dev);
+  return bf16 ? launch<64, true>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, st, dev)
+              : launch<64, false>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, st, dev);
+}
+
 static int run_ws(bool bf16, const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int Sq,
                   int Skv, int hd, int causal, float scale, void* ws, size_t ws_bytes, void* stream) {
   bool empty = false;
@@ -1475,11 +1519,17 @@ static int run_ws(bool bf16, const void* q, const void* k, const void* v, void* 
   if (ds != FA_OK) return ds;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (hd == 128)
-    return bf16 ? launch_sk<128, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, causal, scale, ws, st, dev)
-                : launch_sk<128, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, causal, scale, ws, st, dev);
-  return bf16 ? launch_sk<64, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, causal, scale, ws, st, dev)
-              : launch_sk<64, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, causal, scale, ws, st, dev);
+    return bf16 ? launch_sk<128, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, ws, st, dev)
+                : launch_sk<128, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, ws, st, dev);
+  return bf16 ? launch_sk<64, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, ws, st, dev)
+              : launch_sk<64, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, ws, st, dev);
 }
+
+}  // namespace fa
+
+#include "kv_append.cuh"
+
+namespace fa {
 
 // ==================================== split-KV with library-owned scratch
 //
@@ -1533,6 +1583,7 @@ static int static_scratch(int dev, cudaStream_t stream, uint8_t** base) {
 template <int HD, bool BF16>
 static int launch_sk_static(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int Sq,
                             int Skv, int causal, float scale, uint8_t* base, cudaStream_t stream, int dev) {
+  const int kv_cap = Skv;
   using SL = SkLayout<HD>;
   auto kern = fa_prefill_sk_kernel<HD, BF16>;
   SkParams sp;
@@ -1572,8 +1623,8 @@ static int launch_sk_static(const void* q, const void* k, const void* v, void* o
   EncodeTiledFn enc = encoder();
   if (!enc) return FA_ERR_LAUNCH;
   CUtensorMap mq, mk, mv, mo;
-  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, HD) || !encode_bshd(&mk, enc, k, BF16, B, Skv, Hkv, HD) ||
-      !encode_bshd(&mv, enc, v, BF16, B, Skv, Hkv, HD) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, HD))
+  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, HD, Sq) || !encode_bshd(&mk, enc, k, BF16, B, Skv, Hkv, HD, kv_cap) ||
+      !encode_bshd(&mv, enc, v, BF16, B, Skv, Hkv, HD, kv_cap) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, HD, Sq))
     return FA_ERR_LAUNCH;
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
@@ -1639,6 +1690,18 @@ extern "C" int fa_prefill_ws_bf16(const void* q, const void* k, const void* v, v
 }
 
 extern "C" size_t fa_workspace_bytes(int hd) { return fa::ws_bytes_for(hd); }
+
+extern "C" int fa_prefill_kvcache(const void* q, const void* k_cache, const void* v_cache, void* o, int B, int Hq,
+                                  int Hkv, int Sq, int kv_len, int kv_cap, int hd, int causal, float scale, int bf16,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  return fa::run_kvcache(bf16 != 0, q, k_cache, v_cache, o, B, Hq, Hkv, Sq, kv_len, kv_cap, hd, causal, scale,
+                         workspace, workspace_bytes, stream);
+}
+
+extern "C" int fa_kv_append(const void* k_new, const void* v_new, const void* positions, void* k_cache, void* v_cache,
+                            int B, int T, int Hkv, int hd, int kv_cap, int bf16, void* stream) {
+  return fa::run_kv_append(k_new, v_new, positions, k_cache, v_cache, B, T, Hkv, hd, kv_cap, bf16 != 0, stream);
+}
 
 extern "C" int fa_split_kv_advised(int B, int Hq, int Hkv, int Sq, int Skv, int causal) {
   (void)causal;  // the longest query tile walks all Skv keys either way (bottom-right alignment)

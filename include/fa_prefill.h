@@ -158,6 +158,58 @@ size_t fa_workspace_bytes(int hd);
  */
 int fa_split_kv_advised(int B, int Hq, int Hkv, int Sq, int Skv, int causal);
 
+/*
+ * fa_prefill_kvcache -- attention over a K/V cache, the read side of a
+ * chunked prefill.  q, o as in fa_prefill; k_cache, v_cache are
+ * [B][kv_cap][Hkv][hd] 16-bit, device, of which rows [0, kv_len) of each
+ * sequence hold keys and values.  The Sq query rows are the last Sq of the
+ * kv_len positions (row i sees key j iff j <= kv_len - Sq + i when causal).
+ * Rows kv_len .. kv_cap - 1 never reach the result whatever they hold
+ * (unwritten or stale cache memory): the TMA maps describe kv_len rows with
+ * a batch stride of kv_cap rows, so rows past kv_len are loaded as zeros --
+ * the pages' rule that rows at or past kv_end are zero-staged and must not
+ * contribute (minfer "28 · r23 — f16-path whole-graph wall decomposition +
+ * FA_TKV occupancy raise", section 3.2).
+ *   bf16       0: f16 (as fa_prefill), non-zero: bfloat16
+ *   workspace  NULL: the one-shot kernel; otherwise the split-KV kernel with
+ *              this workspace, under fa_prefill_ws's rules for it
+ * Errors: those of fa_prefill (fa_prefill_ws with a workspace), and
+ * FA_ERR_INVALID_ARG for kv_len > kv_cap, a negative kv_len or kv_cap, or o
+ * overlapping the caches' full kv_cap extent.
+ */
+int fa_prefill_kvcache(const void* q, const void* k_cache, const void* v_cache,
+                       void* o, int B, int Hq, int Hkv, int Sq, int kv_len,
+                       int kv_cap, int hd, int causal, float scale, int bf16,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * fa_kv_append -- the K/V-cache append before a chunked prefill's attention
+ * (the pages' store_kv kernel, minfer "11 · P5 — prefill gap session: TM=128
+ * big tiles + FA rewrite", section 3.2), for K and V in one launch:
+ *     k_cache[b][positions[b][t]][h][:] = round16(k_new[b][t][h][:])
+ * and the same for V, round16 being IEEE round to nearest, ties to even, into
+ * f16 (bf16 == 0) or bfloat16 (bf16 != 0): values past the largest finite
+ * 16-bit value become +-inf, NaN stays NaN.
+ *   k_new, v_new      [B][T][Hkv][hd] f32, device, read-only, 16-byte aligned
+ *   positions         [B][T] int32, device, read-only: each token's cache row
+ *   k_cache, v_cache  [B][kv_cap][Hkv][hd] 16-bit, device, 16-byte aligned;
+ *                     only the rows named by positions are written
+ *   hd                any positive multiple of 8 (the attention takes 64, 128)
+ * A position outside [0, kv_cap) is skipped (nothing written for that token)
+ * and reported in the device status word: fa_debug_status() returns code 32
+ * with the flat index b * T + t of one such token in bits 8-31.  Positions
+ * within a sequence should be distinct; of two tokens naming one row, either
+ * may win.  Asynchronous on `stream` like the attention entry points.
+ * Errors: FA_ERR_INVALID_ARG (null pointer, negative B or T, Hkv < 1,
+ * kv_cap < 1, caches overlapping each other or the inputs),
+ * FA_ERR_UNSUPPORTED (hd not a positive multiple of 8, or more than about
+ * 2^31 8-element groups), FA_ERR_ALIGNMENT, FA_ERR_DEVICE, FA_ERR_LAUNCH.
+ * B == 0 or T == 0 is a no-op returning FA_OK.
+ */
+int fa_kv_append(const void* k_new, const void* v_new, const void* positions,
+                 void* k_cache, void* v_cache, int B, int T, int Hkv, int hd,
+                 int kv_cap, int bf16, void* stream);
+
 /* Size of the library's static device scratch array (one per device the
  * library runs on): 20 MiB, under 0.01 % of a 288 GB GB300. */
 #define FA_STATIC_SCRATCH_BYTES (20u * 1024u * 1024u)
@@ -216,7 +268,8 @@ unsigned int fa_smem_bytes(int hd);
 /*
  * fa_debug_status -- the kernel watchdog word of the current device: 0 when
  * no kernel has reported a problem since the last clear, otherwise a code
- * (bits 0-7: which wait gave up; bits 8-31: the CTA index, saturated).  A
+ * (bits 0-7: which wait gave up -- or 32, a cache-append position out of
+ * range, see fa_kv_append; bits 8-31: the CTA index, saturated).  A
  * pipeline wait that does not complete within the watchdog limit records its
  * code here, makes its CTA skip its remaining work and exit cleanly (no trap),
  * so the context stays usable.  Synchronises the device.  Returns -1 if the

@@ -137,3 +137,28 @@ def test_split_advice_rejects_bad_sizes_without_a_device(fa):
     assert f(-1, 4, 2, 8, 8, 1) == -1
     assert f(0, 4, 2, 8, 8, 1) == 0       # nothing to compute: no advice needed, no device touched
     assert f(1, 4, 2, 8, 0, 1) == 0
+
+
+def test_kvcache_and_append_errors_without_a_device(fa):
+    """The cache entry points check their arguments before any device call."""
+    ap = fa.fa_kv_append
+    ok = dict(kn=A, vn=2 * A, pos=3 * A, kc=4 * A, vc=5 * A, B=1, T=4, Hkv=2, hd=128, cap=16, bf16=0)
+
+    def append(**kw):
+        a = dict(ok, **kw)
+        return ap(a["kn"], a["vn"], a["pos"], a["kc"], a["vc"], a["B"], a["T"], a["Hkv"], a["hd"], a["cap"],
+                  a["bf16"], 0)
+
+    assert append(kn=0) == 1 and append(pos=0) == 1 and append(vc=0) == 1
+    assert append(B=-1) == 1 and append(T=-1) == 1 and append(Hkv=0) == 1 and append(cap=0) == 1
+    assert append(hd=12) == 2 and append(hd=0) == 2
+    assert append(kn=A + 8) == 3 and append(kc=4 * A + 4) == 3 and append(pos=3 * A + 2) == 3
+    assert append(vc=4 * A) == 1                   # caches overlap
+    assert append(B=0) == 0 and append(T=0, kn=0, vn=0, pos=0) == 0
+    kc = fa.fa_prefill_kvcache
+    args = (A, 2 * A, 3 * A, 4 * A, 1, 4, 2, 8)
+    assert kc(*args, 9, 8, 128, 1, 0.1, 0, 0, 0, 0) == 1       # kv_len > kv_cap
+    assert kc(*args, -1, 8, 128, 1, 0.1, 0, 0, 0, 0) == 1
+    assert kc(*args, 8, 16, 96, 1, 0.1, 0, 0, 0, 0) == 2
+    assert kc(*args, 8, 16, 128, 1, 0.1, 1, 5 * A + 16, 1 << 30, 0) == 3   # workspace not 256-aligned
+    assert kc(A, 2 * A, 3 * A, 4 * A, 0, 4, 2, 8, 8, 16, 128, 1, 0.1, 0, 0, 0, 0) == 0  # B = 0
