@@ -201,3 +201,14 @@ def kv_append(k_new, v_new, positions, k_cache_bits, v_cache_bits, bf16: bool):
     if n < 0:
         raise ValueError("bad arguments")
     return int(n)
+
+
+def gather_pages(pool, block_table, kv_len: int, page_size: int):
+    """Contiguous K or V [B, kv_len, Hkv, hd] from a paged pool
+    [num_blocks, page_size, Hkv, hd] and a block table [B, max_pages]: key j
+    of sequence b is pool[block_table[b, j // page_size], j % page_size] (the
+    definition of a paged cache; the attention oracle then runs on the result)."""
+    pool = np.asarray(pool.detach().cpu().double().numpy() if hasattr(pool, "detach") else pool, dtype=np.float64)
+    table = np.asarray(block_table.cpu().numpy() if hasattr(block_table, "cpu") else block_table, dtype=np.int64)
+    j = np.arange(kv_len)
+    return np.ascontiguousarray(pool[table[:, j // page_size], j % page_size])

@@ -419,6 +419,20 @@ def test_kv_append_scatters_rounded_rows_to_positions():
         assert np.array_equal(kc, wk) and np.array_equal(vc, wv)
 
 
+def test_gather_pages_by_brute_force():
+    """The paged-cache gather against a loop over every key: key j of sequence
+    b is row j % page of block table[b][j // page]."""
+    rng = np.random.default_rng(3)
+    nb, page, Hkv, hd, B, kv_len = 9, 4, 2, 3, 2, 11
+    pool = rng.standard_normal((nb, page, Hkv, hd))
+    table = np.stack([rng.permutation(nb)[:3] for _ in range(B)])
+    got = oracle.gather_pages(pool, table, kv_len, page)
+    assert got.shape == (B, kv_len, Hkv, hd)
+    for b in range(B):
+        for j in range(kv_len):
+            assert np.array_equal(got[b, j], pool[table[b, j // page], j % page])
+
+
 # --------------------------------------------------------------------------
 # planted mistakes: each wrong variant of the oracle fails at least one pin
 # --------------------------------------------------------------------------
