@@ -49,6 +49,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--op", choices=["attention", "kv_append"], default="attention",
                     help="attention (the default line) or the K/V-cache append of the workload's whole K/V")
+    ap.add_argument("--page-size", type=int, default=0,
+                    help="read K/V through a paged pool of this page size (a multiple of 128; one-shot kernel)")
     ap.add_argument("--path", choices=["auto", "oneshot", "split"], default="auto",
                     help="kernel: the library's advice for the shape (auto), one-shot, or split-KV")
     return ap.parse_args(argv)
@@ -295,19 +297,45 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     split = (args.path == "split" or
              (args.path == "auto" and fa.split_kv_advised(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.causal)))
-    if split:
+    paged = args.page_size > 0
+    if paged:  # each copy's K/V scattered over a pool in shuffled page order
+        split = False
+        page = args.page_size
+        npg = (w.Skv + page - 1) // page
+        g = torch.Generator(device="cpu")
+        g.manual_seed(w.seed)
+        pcopies = []
+        for dq, dk, dv, do in copies:
+            perm = torch.randperm(w.B * npg, generator=g).reshape(w.B, npg).to(torch.int32)
+            kp = torch.zeros((w.B * npg, page, w.Hkv, w.hd), dtype=dk.dtype, device=dev)
+            vp = torch.zeros_like(kp)
+            for b in range(w.B):
+                for p_ in range(npg):
+                    r0, r1 = p_ * page, min(w.Skv, (p_ + 1) * page)
+                    kp[int(perm[b, p_]), : r1 - r0] = dk[b, r0:r1]
+                    vp[int(perm[b, p_]), : r1 - r0] = dv[b, r0:r1]
+            pcopies.append((dq, kp, vp, perm.to(dev), do))
+        bf = int(w.dtype == "bf16")
+
+        def step(i):
+            dq, kp, vp, tb, do = pcopies[i % ncopy]
+            st = fa.fa_prefill_paged(dq, kp, vp, tb, do, w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.hd, page, npg,
+                                     w.B * npg, int(w.causal), w.scale, bf, stream)
+            if st != 0:
+                raise fa.FaError(st, "fa_prefill_paged")
+    elif split:
         fn = fa.fa_prefill_ws_bf16 if w.dtype == "bf16" else fa.fa_prefill_ws
         ws = torch.zeros(fa.workspace_bytes(w.hd), dtype=torch.uint8, device=dev)  # zero-filled once
         extra = (ws, ws.numel())
     else:
         fn = fa.fa_prefill_bf16 if w.dtype == "bf16" else fa.fa_prefill
         extra = ()
-
-    def step(i):
-        dq, dk, dv, do = copies[i % ncopy]
-        st = fn(dq, dk, dv, do, w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.hd, int(w.causal), w.scale, *extra, stream)
-        if st != 0:
-            raise fa.FaError(st, fn.__name__)
+    if not paged:
+        def step(i):
+            dq, dk, dv, do = copies[i % ncopy]
+            st = fn(dq, dk, dv, do, w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.hd, int(w.causal), w.scale, *extra, stream)
+            if st != 0:
+                raise fa.FaError(st, fn.__name__)
 
     def barrier():
         if world > 1:
@@ -339,7 +367,7 @@ def run_ours(args):
 
     # end to end through the public API: pinned host inputs -> device -> kernel -> host O
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not paged:  # the e2e leg times the contiguous public API only
         hq_, hk_, hv_ = q.pin_memory(), k.pin_memory(), v.pin_memory()
         ho = torch.empty_like(q).pin_memory()
         dq, dk, dv = torch.empty_like(q, device=dev), torch.empty_like(k, device=dev), torch.empty_like(v, device=dev)
@@ -379,7 +407,7 @@ def run_ours(args):
         return 0
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     achieved = flops / (ms_step * 1e-3) / 1e12
-    traffic = recorded_traffic(w.name + (":split" if split else ""))
+    traffic = recorded_traffic(w.name + (":split" if split else "") + (":paged" if paged else ""))
     line = {
         "metric": "causal prefill attention TFLOPS (ms/call, % of dense peak)",
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -390,7 +418,9 @@ def run_ours(args):
                    "flops_per_call": flops, "flop_convention": "4*hd*visible (query,key) pairs",
                    "l2": f"inputs rotated over {ncopy} resident copies ({ncopy * io / 1e6:.0f} MB > L2)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "kernel": "fa_prefill_sk_kernel (split-KV)" if split else "fa_prefill_kernel (one-shot)"},
+                   "kernel": "fa_prefill_sk_kernel (split-KV)" if split else "fa_prefill_kernel (one-shot)",
+                   "kv_layout": f"paged, {args.page_size}-token pages in shuffled order" if paged
+                   else "contiguous BSHD"},
         "pct_of_peak": 100.0 * achieved / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,

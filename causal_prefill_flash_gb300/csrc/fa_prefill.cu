@@ -86,6 +86,7 @@ enum : uint32_t {
   WD_SOFTMAX_O_DONE = 8,
   WD_DRAIN = 9,
   WD_MERGE_FLAG = 12,
+  WD_PAGE_BLOCK = 33,  // a block-table entry outside the pool (its tiles load as zeros)
 };
 
 // Shared-memory plan of one CTA, all offsets from a 1024-byte aligned base.
@@ -122,6 +123,11 @@ struct Params {
   int causal;
   float sl2;       // scale * log2(e)
   unsigned long long watchdog_ns;
+  // paged K/V (one-shot kernel only): K/V tile t of sequence b lives in pool
+  // block block_table[b * max_pages + t * BN / page_size], rows from
+  // (t * BN) % page_size; the last page is read through the tail maps
+  const int* block_table;  // nullptr: contiguous [B][Skv][Hkv][hd] K/V
+  int page_size, max_pages, num_blocks, last_page;
 };
 
 // The two query tiles of one CTA.  Longest tiles first; for head pairs the
@@ -233,6 +239,7 @@ template <int HD, bool BF16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fa_prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                      const __grid_constant__ CUtensorMap tmKt, const __grid_constant__ CUtensorMap tmVt,
                       const Params p) {
   using L = Layout<HD>;
   constexpr int NSLOT = L::NSLOT;
@@ -308,15 +315,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // loads in order K_0, V_0, K_1, V_1, ...; load i goes to slot i % NSLOT
       int issued = 0;
       bool ok = true;
+      int page = -1, blk = 0;  // paged K/V: the pool block of the current page
+      if (p.block_table) {
+        ptx::prefetch_tmap(&tmKt);
+        ptx::prefetch_tmap(&tmVt);
+      }
       for (int i = 0; i < 2 * n; ++i) {
         const int s = i % NSLOT;
         if (i >= NSLOT) ok = wait_bar(bEmpty(s), ((i / NSLOT) & 1) ^ 1u, abort_flag, p.watchdog_ns, WD_PRODUCER_EMPTY);
         if (!ok) break;
+        const int key0 = (i >> 1) * BN;
+        int row = key0, bat = w.b;
+        bool tail = false;
+        if (p.block_table) {
+          const int pg = key0 / p.page_size;
+          if (pg != page) {
+            page = pg;
+            blk = __ldg(p.block_table + static_cast<size_t>(w.b) * p.max_pages + pg);
+            if (blk < 0 || blk >= p.num_blocks) {  // outside the pool: reported, and read one block
+              atomicCAS(&g_fa_status, 0u,   // past the end, where TMA fills zeros
+                        WD_PAGE_BLOCK | ((blockIdx.x < 0xFFFFFFu ? blockIdx.x : 0xFFFFFFu) << 8));
+              blk = p.num_blocks;
+            }
+          }
+          row = key0 - pg * p.page_size;
+          bat = blk;
+          tail = pg == p.last_page;
+        }
         ptx::mbar_arrive_expect_tx(bFull(s), L::SLOT_BYTES);
-        const CUtensorMap* m = (i & 1) ? &tmV : &tmK;
+        const CUtensorMap* m = (i & 1) ? (tail ? &tmVt : &tmV) : (tail ? &tmKt : &tmK);
 #pragma unroll
         for (int c = 0; c < (int)L::KCH; ++c)
-          ptx::tma_load_4d(sRing + s * L::SLOT_BYTES + c * (BN * 128), m, bFull(s), c * 64, w.hk, (i >> 1) * BN, w.b);
+          ptx::tma_load_4d(sRing + s * L::SLOT_BYTES + c * (BN * 128), m, bFull(s), c * 64, w.hk, row, bat);
         ++issued;
       }
       if (!ok) {
@@ -1231,9 +1261,15 @@ static bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return na > 0 && nb > 0 && x < y + nb && y < x + na;
 }
 
+// Paged K/V: pool [num_blocks][page_size][Hkv][hd], block table [B][max_pages].
+struct Paged {
+  const int* table;
+  int page_size, max_pages, num_blocks;
+};
+
 template <int HD, bool BF16>
 static int launch(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int Sq, int Skv,
-                  int kv_cap, int causal, float scale, cudaStream_t stream, int dev) {
+                  int kv_cap, int causal, float scale, cudaStream_t stream, int dev, const Paged* pg = nullptr) {
   using L = Layout<HD>;
   auto kern = fa_prefill_kernel<HD, BF16>;
   const int slot = (HD == 128 ? 2 : 0) + (BF16 ? 1 : 0);
@@ -1246,11 +1282,32 @@ static int launch(const void* q, const void* k, const void* v, void* o, int B, i
   }
   EncodeTiledFn enc = encoder();
   if (!enc) return FA_ERR_LAUNCH;
-  CUtensorMap mq, mk, mv, mo;
-  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, HD, Sq) || !encode_bshd(&mk, enc, k, BF16, B, Skv, Hkv, HD, kv_cap) ||
-      !encode_bshd(&mv, enc, v, BF16, B, Skv, Hkv, HD, kv_cap) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, HD, Sq))
+  CUtensorMap mq, mk, mv, mo, mkt, mvt;
+  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, HD, Sq) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, HD, Sq))
     return FA_ERR_LAUNCH;
+  int last_page = 0;
+  if (pg && Skv > 0) {
+    // whole pages through the pool maps; the last page through maps that end
+    // at its last valid row, so rows past Skv load as zeros
+    last_page = (Skv - 1) / pg->page_size;
+    const int tail_rows = Skv - last_page * pg->page_size;
+    if (!encode_bshd(&mk, enc, k, BF16, pg->num_blocks, pg->page_size, Hkv, HD, pg->page_size) ||
+        !encode_bshd(&mv, enc, v, BF16, pg->num_blocks, pg->page_size, Hkv, HD, pg->page_size) ||
+        !encode_bshd(&mkt, enc, k, BF16, pg->num_blocks, tail_rows, Hkv, HD, pg->page_size) ||
+        !encode_bshd(&mvt, enc, v, BF16, pg->num_blocks, tail_rows, Hkv, HD, pg->page_size))
+      return FA_ERR_LAUNCH;
+  } else {
+    if (!encode_bshd(&mk, enc, k, BF16, B, Skv, Hkv, HD, kv_cap) || !encode_bshd(&mv, enc, v, BF16, B, Skv, Hkv, HD, kv_cap))
+      return FA_ERR_LAUNCH;
+    mkt = mk;
+    mvt = mv;
+  }
   Params prm;
+  prm.block_table = (pg && Skv > 0) ? pg->table : nullptr;
+  prm.page_size = pg ? pg->page_size : 0;
+  prm.max_pages = pg ? pg->max_pages : 0;
+  prm.num_blocks = pg ? pg->num_blocks : 0;
+  prm.last_page = last_page;
   prm.o = static_cast<uint16_t*>(o);
   prm.B = B;
   prm.Hq = Hq;
@@ -1264,7 +1321,7 @@ static int launch(const void* q, const void* k, const void* v, void* o, int B, i
   prm.sl2 = scale * 1.4426950408889634f;
   prm.watchdog_ns = WATCHDOG_NS;
   const long long grid = grid_size(B, Hq, Hkv, Sq);
-  kern<<<dim3((unsigned)grid), dim3(NUM_THREADS), L::REQUEST, stream>>>(mq, mk, mv, mo, prm);
+  kern<<<dim3((unsigned)grid), dim3(NUM_THREADS), L::REQUEST, stream>>>(mq, mk, mv, mo, mkt, mvt, prm);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   return FA_OK;
 }
@@ -1506,6 +1563,40 @@ static int run_kvcache(bool bf16, const void* q, const void* k, const void* v, v
               : launch<64, false>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, st, dev);
 }
 
+// Attention over a paged K/V pool (one-shot kernel).
+static int run_paged(bool bf16, const void* q, const void* k_pool, const void* v_pool, const void* block_table,
+                     void* o, int B, int Hq, int Hkv, int Sq, int kv_len, int hd, int page_size, int max_pages,
+                     int num_blocks, int causal, float scale, void* stream) {
+  if (kv_len < 0 || page_size < BN || page_size % BN != 0 || max_pages < 0 || num_blocks < 1)
+    return FA_ERR_INVALID_ARG;
+  if ((long long)max_pages * page_size < kv_len) return FA_ERR_INVALID_ARG;
+  bool empty = false;
+  const void* k = k_pool;
+  const void* v = v_pool;
+  const int vs = validate(q, k, v, o, B, Hq, Hkv, Sq, kv_len, hd, scale, &empty);
+  if (vs != FA_OK || empty) return vs;
+  if (kv_len > 0) {
+    if (!block_table) return FA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(block_table) & 3u) return FA_ERR_ALIGNMENT;
+    if ((unsigned long long)page_size * Hkv * hd * 2 >= (1ull << 40)) return FA_ERR_UNSUPPORTED;
+    const unsigned long long qn = (unsigned long long)B * Sq * Hq * hd;
+    const unsigned long long pn = (unsigned long long)num_blocks * page_size * Hkv * hd;
+    if (overlaps(o, qn * 2, k, pn * 2) || overlaps(o, qn * 2, v, pn * 2) ||
+        overlaps(o, qn * 2, block_table, (size_t)B * max_pages * 4))
+      return FA_ERR_INVALID_ARG;
+  }
+  int dev = -1;
+  const int ds = check_device(&dev);
+  if (ds != FA_OK) return ds;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Paged pg{static_cast<const int*>(block_table), page_size, max_pages, num_blocks};
+  if (hd == 128)
+    return bf16 ? launch<128, true>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, st, dev, &pg)
+                : launch<128, false>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, st, dev, &pg);
+  return bf16 ? launch<64, true>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, st, dev, &pg)
+              : launch<64, false>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, st, dev, &pg);
+}
+
 static int run_ws(bool bf16, const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int Sq,
                   int Skv, int hd, int causal, float scale, void* ws, size_t ws_bytes, void* stream) {
   bool empty = false;
@@ -1696,6 +1787,13 @@ extern "C" int fa_prefill_kvcache(const void* q, const void* k_cache, const void
                                   void* workspace, size_t workspace_bytes, void* stream) {
   return fa::run_kvcache(bf16 != 0, q, k_cache, v_cache, o, B, Hq, Hkv, Sq, kv_len, kv_cap, hd, causal, scale,
                          workspace, workspace_bytes, stream);
+}
+
+extern "C" int fa_prefill_paged(const void* q, const void* k_pool, const void* v_pool, const void* block_table,
+                                void* o, int B, int Hq, int Hkv, int Sq, int kv_len, int hd, int page_size,
+                                int max_pages, int num_blocks, int causal, float scale, int bf16, void* stream) {
+  return fa::run_paged(bf16 != 0, q, k_pool, v_pool, block_table, o, B, Hq, Hkv, Sq, kv_len, hd, page_size,
+                       max_pages, num_blocks, causal, scale, stream);
 }
 
 extern "C" int fa_kv_append(const void* k_new, const void* v_new, const void* positions, void* k_cache, void* v_cache,

@@ -183,6 +183,34 @@ int fa_prefill_kvcache(const void* q, const void* k_cache, const void* v_cache,
                        void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * fa_prefill_paged -- attention over a paged K/V cache (one-shot kernel).  q,
+ * o as in fa_prefill; K and V live in pools of fixed-size pages:
+ *   k_pool, v_pool  [num_blocks][page_size][Hkv][hd] 16-bit, device
+ *   block_table     [B][max_pages] int32, device: key j of sequence b is row
+ *                   j % page_size of pool block block_table[b][j / page_size]
+ *   kv_len          keys per sequence (the same for every b); the Sq query
+ *                   rows are the last Sq of them (bottom-right causal)
+ *   page_size       a multiple of 128 (one KV tile never spans two pages)
+ *   bf16            0: f16, non-zero: bfloat16
+ * Rows of the last page past kv_len never contribute (they load as zeros).
+ * A block-table entry outside [0, num_blocks) is reported in the device
+ * status word (fa_debug_status() code 33) and its page reads as zeros.  The
+ * pages read K/V through one contiguous row index (kv_end, the query's
+ * absolute position: minfer "28 · r23 — f16-path whole-graph wall
+ * decomposition + FA_TKV occupancy raise", section 3.2); the page
+ * indirection is this library's extension of that index.
+ * Errors: those of fa_prefill, and FA_ERR_INVALID_ARG for a page_size that is
+ * not a positive multiple of 128, max_pages * page_size < kv_len,
+ * num_blocks < 1, a NULL block table (kv_len > 0), or o overlapping a pool or
+ * the table; FA_ERR_ALIGNMENT for a block table not 4-byte aligned.
+ */
+int fa_prefill_paged(const void* q, const void* k_pool, const void* v_pool,
+                     const void* block_table, void* o, int B, int Hq, int Hkv,
+                     int Sq, int kv_len, int hd, int page_size, int max_pages,
+                     int num_blocks, int causal, float scale, int bf16,
+                     void* stream);
+
+/*
  * fa_kv_append -- the K/V-cache append before a chunked prefill's attention
  * (the pages' store_kv kernel, minfer "11 · P5 — prefill gap session: TM=128
  * big tiles + FA rewrite", section 3.2), for K and V in one launch:
@@ -269,7 +297,8 @@ unsigned int fa_smem_bytes(int hd);
  * fa_debug_status -- the kernel watchdog word of the current device: 0 when
  * no kernel has reported a problem since the last clear, otherwise a code
  * (bits 0-7: which wait gave up -- or 32, a cache-append position out of
- * range, see fa_kv_append; bits 8-31: the CTA index, saturated).  A
+ * range (fa_kv_append), or 33, a block-table entry outside the pool
+ * (fa_prefill_paged); bits 8-31: the CTA or token index, saturated).  A
  * pipeline wait that does not complete within the watchdog limit records its
  * code here, makes its CTA skip its remaining work and exit cleanly (no trap),
  * so the context stays usable.  Synchronises the device.  Returns -1 if the

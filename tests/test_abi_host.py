@@ -162,3 +162,21 @@ def test_kvcache_and_append_errors_without_a_device(fa):
     assert kc(*args, 8, 16, 96, 1, 0.1, 0, 0, 0, 0) == 2
     assert kc(*args, 8, 16, 128, 1, 0.1, 1, 5 * A + 16, 1 << 30, 0) == 3   # workspace not 256-aligned
     assert kc(A, 2 * A, 3 * A, 4 * A, 0, 4, 2, 8, 8, 16, 128, 1, 0.1, 0, 0, 0, 0) == 0  # B = 0
+
+
+def test_paged_errors_without_a_device(fa):
+    f = fa.fa_prefill_paged
+    ok = dict(q=A, kp=8 * A, vp=16 * A, bt=24 * A, o=32 * A, B=1, Hq=4, Hkv=2, Sq=8, kv_len=300, hd=128, page=128,
+              maxp=3, nb=4, causal=1, scale=0.1, bf16=0)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["q"], a["kp"], a["vp"], a["bt"], a["o"], a["B"], a["Hq"], a["Hkv"], a["Sq"], a["kv_len"], a["hd"],
+                 a["page"], a["maxp"], a["nb"], a["causal"], a["scale"], a["bf16"], 0)
+
+    assert call(page=64) == 1 and call(page=200) == 1 and call(page=0) == 1   # not a multiple of 128
+    assert call(maxp=2) == 1                      # 2 pages of 128 < 300 keys
+    assert call(nb=0) == 1 and call(bt=0) == 1 and call(kv_len=-1) == 1
+    assert call(bt=24 * A + 2) == 3 and call(hd=96) == 2
+    assert call(o=9 * A) == 1                     # o inside the K pool
+    assert call(B=0) == 0
