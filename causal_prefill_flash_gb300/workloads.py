@@ -89,6 +89,8 @@ WORKLOADS = [
     Workload("longctx_chunk128_kv32768", 1, 32, 8, 128, 32768, 128, seed=1240,
              note="a 128-row chunk over a 32640-token cached context: 16 query-tile pairs, "
                   "each 256 KV tiles long (an underfilled grid), f16"),
+    Workload("encoder_s4096_noncausal", 2, 16, 16, 4096, 4096, 128, causal=False, dtype="bf16", seed=1241,
+             note="encoder-style bidirectional attention (causal = 0): every row sees all 4096 keys, bf16"),
 ]
 BY_NAME = {w.name: w for w in WORKLOADS}
 

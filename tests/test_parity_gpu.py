@@ -10,7 +10,7 @@ result.  The tolerance covers what the kernel rounds on purpose: P rounded to
 pages note the same f32-regrouping drift between tilings, minfer "53 · r50 —
 FA_TKV 32->16 occupancy experiment", section 2).
 
-Small cases compare every output element; the seven workloads at their full
+Small cases compare every output element; the eight workloads at their full
 sizes (in the launch configuration the benchmark times) compare a sample of
 rows the oracle computes one by one.  Edge cases follow the bug classes the
 pages name: tail tiles that need both the local and the global bound (minfer
@@ -228,7 +228,7 @@ def test_runs_on_a_side_stream():
     _check(out.cpu(), want, "f16", "side stream")
 
 
-# ---------------------------------------------------------- the seven workloads
+# ---------------------------------------------------------- the eight workloads
 
 @pytest.mark.parametrize("idx", range(len(W.WORKLOADS)))
 def test_workload_reduced_full_compare(idx, split):
@@ -275,7 +275,7 @@ def test_split_advice_follows_the_grid_fill():
     adv = lambda w: fa.split_kv_advised(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.causal)
     assert adv(W_["longctx_chunk128_kv32768"])
     for name in ("single_head_s256", "prefill7b_s2048", "ragged_s2659_std3", "gqa_s8192_bf16",
-                 "chunked_kv8192_hd128", "chunked_kv8192_hd64"):
+                 "chunked_kv8192_hd128", "chunked_kv8192_hd64", "encoder_s4096_noncausal"):
         assert not adv(W_[name]), name
 
 
