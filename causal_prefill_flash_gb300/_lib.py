@@ -246,7 +246,7 @@ def attention_kvcache(q, k_cache, v_cache, kv_len: int, causal: bool = True, sca
     elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
         raise ValueError("out must be a contiguous CUDA tensor like q")
     if split is None:
-        split = split_kv_advised(B, Hq, Hkv, Sq, kv_len, causal)
+        split = hd != 256 and split_kv_advised(B, Hq, Hkv, Sq, kv_len, causal)
     ws = workspace_for(q.device, hd, stream) if split else None
     st = fa_prefill_kvcache(q, k_cache, v_cache, out, B, Hq, Hkv, Sq, kv_len, kv_cap, hd, int(bool(causal)),
                             scale, int(q.dtype == torch.bfloat16), ws, ws.numel() if ws is not None else 0, stream)
@@ -313,8 +313,8 @@ def attention(q, k, v, causal: bool = True, scale: float | None = None, out=None
         out = torch.empty_like(q)
     elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
         raise ValueError("out must be a contiguous CUDA tensor like q")
-    if split is None:
-        split = split_kv_advised(B, Hq, Hkv, Sq, Skv, causal)
+    if split is None:  # split-KV exists for hd 64 and 128
+        split = hd != 256 and split_kv_advised(B, Hq, Hkv, Sq, Skv, causal)
     if split:
         fn = fa_prefill_ws_bf16 if q.dtype == torch.bfloat16 else fa_prefill_ws
         ws = workspace_for(q.device, hd, stream)

@@ -590,6 +590,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+}  // namespace fa
+
+#include "fa_prefill256.cuh"
+
+namespace fa {
+
 // ================================================ stream-K (split-KV) kernel
 //
 // The one-shot kernel above gives every CTA whole query-tile pairs, so a grid
@@ -1229,6 +1235,7 @@ static std::atomic<int> g_dev_ok[MAX_DEVICES];
 static std::atomic<int> g_dev_sms[MAX_DEVICES];
 static std::atomic<int> g_attr_set[MAX_DEVICES][4];
 static std::atomic<int> g_sk_attr_set[MAX_DEVICES][4];
+static std::atomic<int> g_attr256_set[MAX_DEVICES][2];
 
 static int check_device(int* dev_out) {
   int dev = -1;
@@ -1249,7 +1256,9 @@ static int check_device(int* dev_out) {
     }
     g_dev_sms[dev].store(sms > 0 ? sms : 1);
     if (major != 10 || minor != 3) st = -FA_ERR_DEVICE;
-    else if ((unsigned)optin < Layout<128>::REQUEST || (unsigned)optin < SkLayout<128>::REQUEST) st = -FA_ERR_SMEM;
+    else if ((unsigned)optin < Layout<128>::REQUEST || (unsigned)optin < SkLayout<128>::REQUEST ||
+             (unsigned)optin < Layout256::REQUEST)
+      st = -FA_ERR_SMEM;
     else st = 1;
     g_dev_ok[dev].store(st);
   }
@@ -1326,6 +1335,45 @@ static int launch(const void* q, const void* k, const void* v, void* o, int B, i
   return FA_OK;
 }
 
+// hd = 256: one query tile per CTA (fa_prefill256_kernel).
+template <bool BF16>
+static int launch256(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int Sq, int Skv,
+                     int kv_cap, int causal, float scale, cudaStream_t stream, int dev) {
+  using L = Layout256;
+  auto kern = fa_prefill256_kernel<BF16>;
+  if (g_attr256_set[dev][BF16 ? 1 : 0].load() == 0) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::REQUEST) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return FA_ERR_SMEM;
+    }
+    g_attr256_set[dev][BF16 ? 1 : 0].store(1);
+  }
+  EncodeTiledFn enc = encoder();
+  if (!enc) return FA_ERR_LAUNCH;
+  CUtensorMap mq, mk, mv, mo;
+  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, L::HD, Sq) || !encode_bshd(&mk, enc, k, BF16, B, Skv, Hkv, L::HD, kv_cap) ||
+      !encode_bshd(&mv, enc, v, BF16, B, Skv, Hkv, L::HD, kv_cap) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, L::HD, Sq))
+    return FA_ERR_LAUNCH;
+  Params prm;
+  std::memset(&prm, 0, sizeof(prm));
+  prm.o = static_cast<uint16_t*>(o);
+  prm.B = B;
+  prm.Hq = Hq;
+  prm.Hkv = Hkv;
+  prm.Sq = Sq;
+  prm.Skv = Skv;
+  prm.G = Hq / Hkv;
+  prm.n_qtiles = (Sq + BM - 1) / BM;
+  prm.causal = causal ? 1 : 0;
+  prm.sl2 = scale * 1.4426950408889634f;
+  prm.watchdog_ns = WATCHDOG_NS;
+  const long long grid = (long long)prm.n_qtiles * Hq * B;
+  if (grid > 0x7FFFFFFFLL) return FA_ERR_UNSUPPORTED;
+  kern<<<dim3((unsigned)grid), dim3(NUM_THREADS_256), L::REQUEST, stream>>>(mq, mk, mv, mo, prm);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  return FA_OK;
+}
+
 // Argument checks shared by every entry point (no device call).  May replace
 // k and v by q when Skv == 0 (no key is ever loaded; the maps need a base).
 static int validate(const void* q, const void*& k, const void*& v, const void* o, int B, int Hq, int Hkv, int Sq,
@@ -1334,7 +1382,7 @@ static int validate(const void* q, const void*& k, const void*& v, const void* o
   if (B < 0 || Sq < 0 || Skv < 0 || Hq < 1 || Hkv < 1) return FA_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
-  if (hd != 64 && hd != 128) return FA_ERR_UNSUPPORTED;
+  if (hd != 64 && hd != 128 && hd != 256) return FA_ERR_UNSUPPORTED;
   if (B == 0 || Sq == 0) {  // nothing to compute; no pointer is read
     *empty = true;
     return FA_OK;
@@ -1366,6 +1414,9 @@ static int run(bool bf16, const void* q, const void* k, const void* v, void* o, 
   const int ds = check_device(&dev);
   if (ds != FA_OK) return ds;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (hd == 256)
+    return bf16 ? launch256<true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev)
+                : launch256<false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev);
   if (hd == 128)
     return bf16 ? launch<128, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev)
                 : launch<128, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev);
@@ -1541,6 +1592,7 @@ static int run_kvcache(bool bf16, const void* q, const void* k, const void* v, v
   const unsigned long long cn = (unsigned long long)B * kv_cap * Hkv * hd;
   if (kv_len > 0 && (overlaps(o, qn * 2, k, cn * 2) || overlaps(o, qn * 2, v, cn * 2))) return FA_ERR_INVALID_ARG;
   if (ws) {
+    if (hd == 256) return FA_ERR_UNSUPPORTED;  // split-KV: hd 64 and 128
     if (reinterpret_cast<uintptr_t>(ws) & 255u) return FA_ERR_ALIGNMENT;
     if (ws_bytes < ws_bytes_for(hd)) return FA_ERR_INVALID_ARG;
   }
@@ -1549,6 +1601,9 @@ static int run_kvcache(bool bf16, const void* q, const void* k, const void* v, v
   if (ds != FA_OK) return ds;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int stride = kv_len > 0 ? kv_cap : 0;  // kv_len == 0: the maps point at q (no key is loaded)
+  if (hd == 256)
+    return bf16 ? launch256<true>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, st, dev)
+                : launch256<false>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, st, dev);
   if (ws) {
     if (hd == 128)
       return bf16 ? launch_sk<128, true>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, ws, st, dev)
@@ -1575,6 +1630,7 @@ static int run_paged(bool bf16, const void* q, const void* k_pool, const void* v
   const void* v = v_pool;
   const int vs = validate(q, k, v, o, B, Hq, Hkv, Sq, kv_len, hd, scale, &empty);
   if (vs != FA_OK || empty) return vs;
+  if (hd == 256) return FA_ERR_UNSUPPORTED;  // hd 256: the one-shot kernel only
   if (kv_len > 0) {
     if (!block_table) return FA_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(block_table) & 3u) return FA_ERR_ALIGNMENT;
@@ -1602,6 +1658,7 @@ static int run_ws(bool bf16, const void* q, const void* k, const void* v, void* 
   bool empty = false;
   const int vs = validate(q, k, v, o, B, Hq, Hkv, Sq, Skv, hd, scale, &empty);
   if (vs != FA_OK || empty) return vs;
+  if (hd == 256) return FA_ERR_UNSUPPORTED;  // hd 256: the one-shot kernel only
   if (!ws) return FA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(ws) & 255u) return FA_ERR_ALIGNMENT;
   if (ws_bytes < ws_bytes_for(hd)) return FA_ERR_INVALID_ARG;
@@ -1740,6 +1797,7 @@ static int run_static(bool bf16, const void* q, const void* k, const void* v, vo
   bool empty = false;
   const int vs = validate(q, k, v, o, B, Hq, Hkv, Sq, Skv, hd, scale, &empty);
   if (vs != FA_OK || empty) return vs;
+  if (hd == 256) return FA_ERR_UNSUPPORTED;  // hd 256: the one-shot kernel only
   int dev = -1;
   const int ds = check_device(&dev);
   if (ds != FA_OK) return ds;
@@ -1834,6 +1892,7 @@ extern "C" const char* fa_status_string(int status) {
 }
 
 extern "C" unsigned int fa_smem_bytes(int hd) {
+  if (hd == 256) return fa::Layout256::REQUEST;
   if (hd == 128) return fa::Layout<128>::REQUEST;
   if (hd == 64) return fa::Layout<64>::REQUEST;
   return 0u;

@@ -91,6 +91,8 @@ WORKLOADS = [
                   "each 256 KV tiles long (an underfilled grid), f16"),
     Workload("encoder_s4096_noncausal", 2, 16, 16, 4096, 4096, 128, causal=False, dtype="bf16", seed=1241,
              note="encoder-style bidirectional attention (causal = 0): every row sees all 4096 keys, bf16"),
+    Workload("gqa_s4096_hd256_bf16", 1, 16, 8, 4096, 4096, 256, dtype="bf16", seed=1242,
+             note="head dimension 256 (16 query heads over 8 KV heads, the shape of 256-wide-head models), bf16"),
 ]
 BY_NAME = {w.name: w for w in WORKLOADS}
 

@@ -34,8 +34,11 @@
  * scale multiplies Q K^T before the mask and the softmax; it must be finite and
  * > 0 (1/sqrt(hd) is the usual value).
  *
- * Supported: hd in {64, 128}; any B, Sq, Skv >= 0 and Hq, Hkv >= 1 whose
- * tensors fit TMA's 32-bit coordinates.  B == 0 or Sq == 0 is a no-op
+ * Supported: hd in {64, 128, 256} (hd 256 on the one-shot kernel: fa_prefill,
+ * fa_prefill_bf16, fa_prefill_kvcache without a workspace; the split-KV, paged
+ * and static-scratch entry points take 64 and 128); any B, Sq, Skv >= 0 and
+ * Hq, Hkv >= 1 whose tensors fit TMA's 32-bit coordinates.  B == 0 or Sq == 0
+ * is a no-op
  * returning FA_OK (the pointers may then be NULL: nothing is read or written);
  * Skv == 0 writes O = 0 (k and v may then be NULL).
  *
@@ -72,7 +75,7 @@ typedef enum {
                                 negative size, Hq or Hkv < 1,
                                 Hq % Hkv != 0, non-finite or <= 0 scale,
                                 o overlapping q/k/v                        */
-    FA_ERR_UNSUPPORTED = 2,  /* hd not in {64, 128}, or a tensor too large
+    FA_ERR_UNSUPPORTED = 2,  /* hd not supported by the entry point, or a tensor too large
                                 for TMA's 32-bit coordinates               */
     FA_ERR_ALIGNMENT = 3,    /* a pointer not 16-byte aligned (TMA rule)  */
     FA_ERR_SMEM = 4,         /* the kernel's shared-memory request does not
@@ -222,7 +225,7 @@ int fa_prefill_paged(const void* q, const void* k_pool, const void* v_pool,
  *   positions         [B][T] int32, device, read-only: each token's cache row
  *   k_cache, v_cache  [B][kv_cap][Hkv][hd] 16-bit, device, 16-byte aligned;
  *                     only the rows named by positions are written
- *   hd                any positive multiple of 8 (the attention takes 64, 128)
+ *   hd                any positive multiple of 8 (the attention takes 64, 128, 256)
  * A position outside [0, kv_cap) is skipped (nothing written for that token)
  * and reported in the device status word: fa_debug_status() returns code 32
  * with the flat index b * T + t of one such token in bits 8-31.  Positions
@@ -284,7 +287,7 @@ const char* fa_status_string(int status);
 
 /*
  * fa_smem_bytes -- the dynamic shared memory one CTA of the kernel requests
- * for head dimension hd (64 or 128), computed from the kernel's own tile
+ * for head dimension hd (64, 128 or 256), computed from the kernel's own tile
  * layout (Q tile, K/V stage ring, P tile, barriers, alignment slack).  Returns
  * 0 for an unsupported hd.  Host-only; no device is touched.  Exposed so the
  * launcher's request can be checked against the layout, the failure class of

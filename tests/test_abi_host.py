@@ -58,6 +58,8 @@ def test_smem_request_matches_the_tile_layout(fa):
         assert fa.smem_bytes(hd) == want
         assert want <= 227 * 1024
     assert fa.smem_bytes(96) == 0
+    # hd 256: one 64 KB query tile, a ring of five 32 KB half tiles, 18 barriers
+    assert fa.smem_bytes(256) == 64 * 1024 + 5 * 32 * 1024 + 18 * 8 + 16 + 1024 <= 227 * 1024
 
 
 A = 0x10000  # aligned fake device addresses: validation fails before any use
@@ -78,7 +80,7 @@ def test_argument_errors_without_a_device(fa, fn):
     assert call(B=-1) == 1 and call(Sq=-3) == 1 and call(Skv=-1) == 1
     assert call(Hq=0) == 1 and call(Hkv=0) == 1 and call(Hkv=3) == 1
     assert call(scale=float("nan")) == 1 and call(scale=0.0) == 1 and call(scale=-1.0) == 1
-    assert call(hd=96) == 2 and call(hd=256) == 2
+    assert call(hd=96) == 2 and call(hd=512) == 2 and call(hd=32) == 2
     assert call(q=A + 8) == 3 and call(o=4 * A + 2) == 3
     assert call(o=A) == 1  # o overlaps q
     assert call(Sq=2 ** 31 - 100) == 2

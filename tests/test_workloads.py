@@ -6,7 +6,7 @@ from causal_prefill_flash_gb300 import workloads as W
 
 def test_table_shapes_and_counts():
     names = [w.name for w in W.WORKLOADS]
-    assert len(names) == len(set(names)) == 8
+    assert len(names) == len(set(names)) == 9
     c = {w.name: w for w in W.WORKLOADS}
     # algorithmic FLOPs = 4 * hd * visible (row, key) pairs
     assert c["single_head_s256"].flops() == 4 * 128 * (256 * 257 // 2)
@@ -21,6 +21,7 @@ def test_table_shapes_and_counts():
     assert c["longctx_chunk128_kv32768"].flops() == 4 * 128 * 32 * sum(32641 + i for i in range(128))
     # no mask: every row sees every key
     assert c["encoder_s4096_noncausal"].flops() == 4 * 128 * 2 * 16 * 4096 * 4096
+    assert c["gqa_s4096_hd256_bf16"].flops() == 4 * 256 * 16 * (4096 * 4097 // 2)
 
 
 def test_inputs_are_seeded_and_typed():
