@@ -52,6 +52,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <utility>
 #include <vector>
 
 #include "fa_prefill.h"
@@ -295,6 +296,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = misc[0];
+  // the set-up above overlaps the previous kernel's tail; nothing in global
+  // memory is read or written before that kernel has completed
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
 
   if (warp >= MMA_WARP) {
   ptx::setmaxnreg_dec<REGS_CONTROL>();
@@ -1270,6 +1275,26 @@ static bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return na > 0 && nb > 0 && x < y + nb && y < x + na;
 }
 
+// Launch with programmatic stream serialization: the kernel's set-up (barrier
+// init, TMEM allocation) may overlap the previous kernel in the stream; the
+// kernel waits (griddepcontrol.wait) before it reads or writes global memory,
+// so it still sees everything the previous kernel wrote.
+template <typename... P, typename... A>
+static cudaError_t launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, A&&... args) {
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<A>(args)...);
+}
+
 // Paged K/V: pool [num_blocks][page_size][Hkv][hd], block table [B][max_pages].
 struct Paged {
   const int* table;
@@ -1330,8 +1355,11 @@ static int launch(const void* q, const void* k, const void* v, void* o, int B, i
   prm.sl2 = scale * 1.4426950408889634f;
   prm.watchdog_ns = WATCHDOG_NS;
   const long long grid = grid_size(B, Hq, Hkv, Sq);
-  kern<<<dim3((unsigned)grid), dim3(NUM_THREADS), L::REQUEST, stream>>>(mq, mk, mv, mo, mkt, mvt, prm);
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  if (launch_pdl(kern, dim3((unsigned)grid), dim3(NUM_THREADS), L::REQUEST, stream, mq, mk, mv, mo, mkt, mvt, prm) !=
+      cudaSuccess) {
+    (void)cudaGetLastError();
+    return FA_ERR_LAUNCH;
+  }
   return FA_OK;
 }
 
@@ -1369,8 +1397,11 @@ static int launch256(const void* q, const void* k, const void* v, void* o, int B
   prm.watchdog_ns = WATCHDOG_NS;
   const long long grid = (long long)prm.n_qtiles * Hq * B;
   if (grid > 0x7FFFFFFFLL) return FA_ERR_UNSUPPORTED;
-  kern<<<dim3((unsigned)grid), dim3(NUM_THREADS_256), L::REQUEST, stream>>>(mq, mk, mv, mo, prm);
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  if (launch_pdl(kern, dim3((unsigned)grid), dim3(NUM_THREADS_256), L::REQUEST, stream, mq, mk, mv, mo, prm) !=
+      cudaSuccess) {
+    (void)cudaGetLastError();
+    return FA_ERR_LAUNCH;
+  }
   return FA_OK;
 }
 

@@ -119,6 +119,9 @@ __global__ void __launch_bounds__(NUM_THREADS_256, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = misc[0];
+  // set-up overlaps the previous kernel's tail; global memory only after it
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
 
   if (warp == PRODUCER_WARP_256) {
     // -------------------------------------------------------------- producer

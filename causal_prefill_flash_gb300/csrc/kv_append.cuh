@@ -29,6 +29,8 @@ __global__ void __launch_bounds__(APPEND_THREADS)
                      int BT, int T, int groups, int cap) {
   // item i: group g = i % groups of row i / groups; rows [0, BT) are K, [BT, 2 BT) are V
   const int total = 2 * BT * groups;
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();  // the previous kernel (e.g. the K/V projection) has completed
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
     const int row = i / groups;
     const int g = i - row * groups;
@@ -85,11 +87,15 @@ static int run_kv_append(const void* k_new, const void* v_new, const void* posit
   const int* ps = static_cast<const int*>(positions);
   uint4* kc = static_cast<uint4*>(k_cache);
   uint4* vc = static_cast<uint4*>(v_cache);
-  if (bf16)
-    kv_append_kernel<true><<<grid, APPEND_THREADS, 0, st>>>(kn, vn, ps, kc, vc, (int)bt, T, (int)groups, cap);
-  else
-    kv_append_kernel<false><<<grid, APPEND_THREADS, 0, st>>>(kn, vn, ps, kc, vc, (int)bt, T, (int)groups, cap);
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  const int bti = static_cast<int>(bt), gi = static_cast<int>(groups);
+  const cudaError_t e =
+      bf16 ? launch_pdl(kv_append_kernel<true>, dim3(grid), dim3(APPEND_THREADS), 0, st, kn, vn, ps, kc, vc, bti, T, gi, cap)
+           : launch_pdl(kv_append_kernel<false>, dim3(grid), dim3(APPEND_THREADS), 0, st, kn, vn, ps, kc, vc, bti, T, gi,
+                        cap);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return FA_ERR_LAUNCH;
+  }
   return FA_OK;
 }
 

@@ -87,6 +87,13 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 // Waits until the shared-memory sources of all committed bulk stores have been read.
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
+// Programmatic dependent launch: let the next kernel in the stream be
+// scheduled (its CTAs start once every CTA of this grid has signalled or
+// exited), and wait until the previous kernel in the stream has completed and
+// its memory is visible (returns at once when the launch did not opt in).
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Warm L2 with a 4-D tensor box (no shared-memory destination, no completion).
 __device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap* m, int c0, int c1, int c2, int c3) {
   asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
