@@ -469,9 +469,14 @@ def run_append(args):
                torch.empty((B, T, Hkv, hd), dtype=dt, device=dev)) for _ in range(ncopy)]
     stream = torch.cuda.current_stream(dev)
 
+    # arguments marshalled once: a call costs the C entry point, not Python
+    lib = fa.load()
+    sp = int(stream.cuda_stream)
+    bf = int(dt == torch.bfloat16)
+    argv = [tuple(t.data_ptr() for t in c) + (B, T, Hkv, hd, T, bf, sp) for c in copies]
+
     def step(i):
-        kn, vn, ps, kc, vc = copies[i % ncopy]
-        st = fa.fa_kv_append(kn, vn, ps, kc, vc, B, T, Hkv, hd, T, int(dt == torch.bfloat16), stream)
+        st = lib.fa_kv_append(*argv[i % ncopy])
         if st != 0:
             raise fa.FaError(st, "fa_kv_append")
 
@@ -499,7 +504,8 @@ def run_append(args):
                    "bytes_per_step": step_bytes,
                    "l2": f"inputs rotated over {ncopy} copies ({ncopy * step_bytes / 1e6:.0f} MB > L2)"},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-                     "peak_source": f"{peak_src} copy bandwidth", "traffic": None},
+                     "peak_source": f"{peak_src} copy bandwidth",
+                     "traffic": recorded_traffic(w.name + ":append")},
         "clocks": clocks.summary(), "gpu_launches": args.steps, "watchdog_status": fa.debug_status(),
     }
     print(json.dumps(line), flush=True)
