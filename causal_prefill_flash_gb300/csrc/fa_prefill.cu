@@ -27,8 +27,9 @@
 //   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: one thread per
 //              query row == TMEM lane; mask only on diagonal / tail tiles; online
 //              max / exp2 / sum; lazy O rescale in TMEM (only when the running
-//              max grew by more than 2^8); P back to TMEM; finally O / l to
-//              global memory.
+//              max grew by more than 2^8); P back to TMEM; finally O / l,
+//              staged 128-byte swizzled in a ring slot the finished tile no
+//              longer needs and written out by TMA tensor stores.
 //
 // TMEM (512 columns): S_A | S_B | O_A | O_B.  Because every MMA of the CTA is
 // issued by one thread and tcgen05 MMAs complete in issue order, S_X(j+1)
@@ -37,10 +38,19 @@
 // rescale never needs an extra wait.
 //
 // KV tiles entirely above the diagonal are never loaded (causal block skip),
-// and the grid runs the longest query tiles first.  Every pipeline wait is
-// bounded by a watchdog: a wait that does not complete records a code in
-// g_fa_status, tells its CTA to stop, and the CTA drains its in-flight copies
-// and MMAs, frees its TMEM and exits (no trap, no hang).
+// and the grid runs the longest query tiles first.  The producer can also read
+// K/V through a block table (paged cache) or from a cache whose capacity
+// exceeds its valid length; only its TMA coordinates change.  Every pipeline
+// wait is bounded by a watchdog: a wait that does not complete records a code
+// in g_fa_status, tells its CTA to stop, and the CTA drains its in-flight
+// copies and MMAs, frees its TMEM and exits (no trap, no hang).  Launches use
+// programmatic dependent launch: set-up overlaps the previous kernel's tail,
+// global memory is touched only after griddepcontrol.wait.
+//
+// The same translation unit holds the other kernels of the library, which
+// share these helpers: the persistent split-KV kernel (fa_prefill_sk_kernel,
+// below), the hd = 256 kernel (fa_prefill256.cuh) and the K/V-cache append
+// (kv_append.cuh).
 
 #include <cuda.h>
 #include <cuda_bf16.h>
