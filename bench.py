@@ -50,7 +50,7 @@ def parse_args(argv=None):
     ap.add_argument("--op", choices=["attention", "kv_append"], default="attention",
                     help="attention (the default line) or the K/V-cache append of the workload's whole K/V")
     ap.add_argument("--page-size", type=int, default=0,
-                    help="read K/V through a paged pool of this page size (a multiple of 128; one-shot kernel)")
+                    help="read K/V through a paged pool of this page size (a multiple of 128)")
     ap.add_argument("--path", choices=["auto", "oneshot", "split"], default="auto",
                     help="kernel: the library's advice for the shape (auto), one-shot, or split-KV")
     return ap.parse_args(argv)
@@ -299,7 +299,6 @@ def run_ours(args):
              (args.path == "auto" and fa.split_kv_advised(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.causal)))
     paged = args.page_size > 0
     if paged:  # each copy's K/V scattered over a pool in shuffled page order
-        split = False
         page = args.page_size
         npg = (w.Skv + page - 1) // page
         g = torch.Generator(device="cpu")
@@ -316,11 +315,16 @@ def run_ours(args):
                     vp[int(perm[b, p_]), : r1 - r0] = dv[b, r0:r1]
             pcopies.append((dq, kp, vp, perm.to(dev), do))
         bf = int(w.dtype == "bf16")
+        pws = torch.zeros(fa.workspace_bytes(w.hd), dtype=torch.uint8, device=dev) if split else None
 
         def step(i):
             dq, kp, vp, tb, do = pcopies[i % ncopy]
-            st = fa.fa_prefill_paged(dq, kp, vp, tb, do, w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.hd, page, npg,
-                                     w.B * npg, int(w.causal), w.scale, bf, stream)
+            if split:
+                st = fa.fa_prefill_paged_ws(dq, kp, vp, tb, do, w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.hd, page, npg,
+                                            w.B * npg, int(w.causal), w.scale, bf, pws, pws.numel(), stream)
+            else:
+                st = fa.fa_prefill_paged(dq, kp, vp, tb, do, w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.hd, page, npg,
+                                         w.B * npg, int(w.causal), w.scale, bf, stream)
             if st != 0:
                 raise fa.FaError(st, "fa_prefill_paged")
     elif split:

@@ -38,6 +38,7 @@ _SIG = {
                                 ctypes.c_size_t, _P]),
     "fa_kv_append": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "fa_prefill_paged": (_I, [_P, _P, _P, _P, _P] + [_I] * 10 + [ctypes.c_float, _I, _P]),
+    "fa_prefill_paged_ws": (_I, [_P, _P, _P, _P, _P] + [_I] * 10 + [ctypes.c_float, _I, _P, ctypes.c_size_t, _P]),
     "fa_prefill_ws_static": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _I, _P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_smem_bytes": (ctypes.c_uint, [_I]),
@@ -158,12 +159,23 @@ def fa_prefill_paged(q, k_pool, v_pool, block_table, o, B, Hq, Hkv, Sq, kv_len, 
                                        _stream(stream)))
 
 
+def fa_prefill_paged_ws(q, k_pool, v_pool, block_table, o, B, Hq, Hkv, Sq, kv_len, hd, page_size, max_pages,
+                        num_blocks, causal, scale, bf16, workspace, workspace_bytes, stream=None) -> int:
+    """Split-KV attention over a paged K/V pool: the C function's arguments. Returns the status."""
+    return int(load().fa_prefill_paged_ws(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table), _ptr(o),
+                                          int(B), int(Hq), int(Hkv), int(Sq), int(kv_len), int(hd),
+                                          int(page_size), int(max_pages), int(num_blocks), int(causal),
+                                          float(scale), int(bf16), _ptr(workspace), int(workspace_bytes),
+                                          _stream(stream)))
+
+
 def attention_paged(q, k_pool, v_pool, block_table, kv_len: int, causal: bool = True,
-                    scale: float | None = None, out=None, stream=None):
+                    scale: float | None = None, out=None, stream=None, split: bool | None = None):
     """O = softmax(scale Q K^T + causal mask) V with K, V read from pools
     [num_blocks, page_size, Hkv, hd] through block_table [B, max_pages]
     (int32): key j of sequence b is k_pool[block_table[b, j // page_size],
-    j % page_size].  page_size must be a multiple of 128.  Raises FaError."""
+    j % page_size].  page_size must be a multiple of 128.  ``split`` as in
+    ``attention`` (split-KV for hd 64 and 128).  Raises FaError."""
     import torch
     if q.dim() != 4 or k_pool.dim() != 4 or v_pool.shape != k_pool.shape or block_table.dim() != 2:
         raise ValueError("q [B, Sq, Hq, hd], pools [num_blocks, page_size, Hkv, hd], table [B, max_pages]")
@@ -184,11 +196,19 @@ def attention_paged(q, k_pool, v_pool, block_table, kv_len: int, causal: bool = 
         out = torch.empty_like(q)
     elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
         raise ValueError("out must be a contiguous CUDA tensor like q")
-    st = fa_prefill_paged(q, k_pool, v_pool, block_table, out, B, Hq, Hkv, Sq, kv_len, hd, page_size,
-                          block_table.shape[1], num_blocks, int(bool(causal)), scale,
-                          int(q.dtype == torch.bfloat16), stream)
+    if split is None:
+        split = hd != 256 and split_kv_advised(B, Hq, Hkv, Sq, kv_len, causal)
+    if split:
+        ws = workspace_for(q.device, hd, stream)
+        st = fa_prefill_paged_ws(q, k_pool, v_pool, block_table, out, B, Hq, Hkv, Sq, kv_len, hd, page_size,
+                                 block_table.shape[1], num_blocks, int(bool(causal)), scale,
+                                 int(q.dtype == torch.bfloat16), ws, ws.numel(), stream)
+    else:
+        st = fa_prefill_paged(q, k_pool, v_pool, block_table, out, B, Hq, Hkv, Sq, kv_len, hd, page_size,
+                              block_table.shape[1], num_blocks, int(bool(causal)), scale,
+                              int(q.dtype == torch.bfloat16), stream)
     if st != FA_OK:
-        raise FaError(st, "fa_prefill_paged")
+        raise FaError(st, "fa_prefill_paged_ws" if split else "fa_prefill_paged")
     return out
 
 

@@ -719,6 +719,7 @@ template <int HD, bool BF16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fa_prefill_sk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                         const __grid_constant__ CUtensorMap tmKt, const __grid_constant__ CUtensorMap tmVt,
                          const __grid_constant__ SkParams sp) {
   const Params& p = sp.p;
   using L = Layout<HD>;
@@ -790,6 +791,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::prefetch_tmap(&tmK);
       ptx::prefetch_tmap(&tmV);
       ptx::prefetch_tmap(&tmO);
+      if (p.block_table) {
+        ptx::prefetch_tmap(&tmKt);
+        ptx::prefetch_tmap(&tmVt);
+      }
       int g = 0;   // loads issued into the ring
       int nq = 0;  // segments whose Q was loaded
       bool ok = true;
@@ -818,15 +823,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (w2.has1) ptx::tma_prefetch_l2_4d(&tmQ, c * 64, w2.hq1, w2.q01, w2.b);
           }
         }
+        int page = -1, blk = 0;  // paged K/V: the pool block of the current page
         for (int i = 2 * jb; i < 2 * je; ++i, ++g) {
           const int s = g % NSLOT;
           if (g >= NSLOT) ok = wait_bar(bEmpty(s), ((g / NSLOT) & 1) ^ 1u, abort_flag, p.watchdog_ns, WD_PRODUCER_EMPTY);
           if (!ok) break;
+          const int key0 = (i >> 1) * BN;
+          int row = key0, bat = w.b;
+          bool tail = false;
+          if (p.block_table) {  // as in the one-shot producer
+            const int pg = key0 / p.page_size;
+            if (pg != page) {
+              page = pg;
+              blk = __ldg(p.block_table + static_cast<size_t>(w.b) * p.max_pages + pg);
+              if (blk < 0 || blk >= p.num_blocks) {
+                atomicCAS(&g_fa_status, 0u,
+                          WD_PAGE_BLOCK | ((blockIdx.x < 0xFFFFFFu ? blockIdx.x : 0xFFFFFFu) << 8));
+                blk = p.num_blocks;
+              }
+            }
+            row = key0 - pg * p.page_size;
+            bat = blk;
+            tail = pg == p.last_page;
+          }
           ptx::mbar_arrive_expect_tx(bFull(s), L::SLOT_BYTES);
-          const CUtensorMap* m = (i & 1) ? &tmV : &tmK;
+          const CUtensorMap* m = (i & 1) ? (tail ? &tmVt : &tmV) : (tail ? &tmKt : &tmK);
 #pragma unroll
           for (int c = 0; c < (int)L::KCH; ++c)
-            ptx::tma_load_4d(sRing + s * L::SLOT_BYTES + c * (BN * 128), m, bFull(s), c * 64, w.hk, (i >> 1) * BN, w.b);
+            ptx::tma_load_4d(sRing + s * L::SLOT_BYTES + c * (BN * 128), m, bFull(s), c * 64, w.hk, row, bat);
         }
       }
       if (!ok) {
@@ -1311,6 +1335,38 @@ struct Paged {
   int page_size, max_pages, num_blocks;
 };
 
+// K/V maps for the producers, and the paged fields of Params.  Contiguous:
+// Skv rows per sequence with a batch stride of kv_cap rows (the tail maps
+// repeat the main ones).  Paged: whole pages through the pool maps, the last
+// page through maps that end at its last valid row, so rows past Skv load as
+// zeros.
+static bool encode_kv(CUtensorMap* mk, CUtensorMap* mv, CUtensorMap* mkt, CUtensorMap* mvt, EncodeTiledFn enc,
+                      const void* k, const void* v, bool bf16, int B, int Skv, int kv_cap, int Hkv, int hd,
+                      const Paged* pg, Params* prm) {
+  prm->block_table = nullptr;
+  prm->page_size = prm->max_pages = prm->num_blocks = prm->last_page = 0;
+  if (pg && Skv > 0) {
+    const int last_page = (Skv - 1) / pg->page_size;
+    const int tail_rows = Skv - last_page * pg->page_size;
+    if (!encode_bshd(mk, enc, k, bf16, pg->num_blocks, pg->page_size, Hkv, hd, pg->page_size) ||
+        !encode_bshd(mv, enc, v, bf16, pg->num_blocks, pg->page_size, Hkv, hd, pg->page_size) ||
+        !encode_bshd(mkt, enc, k, bf16, pg->num_blocks, tail_rows, Hkv, hd, pg->page_size) ||
+        !encode_bshd(mvt, enc, v, bf16, pg->num_blocks, tail_rows, Hkv, hd, pg->page_size))
+      return false;
+    prm->block_table = pg->table;
+    prm->page_size = pg->page_size;
+    prm->max_pages = pg->max_pages;
+    prm->num_blocks = pg->num_blocks;
+    prm->last_page = last_page;
+    return true;
+  }
+  if (!encode_bshd(mk, enc, k, bf16, B, Skv, Hkv, hd, kv_cap) || !encode_bshd(mv, enc, v, bf16, B, Skv, Hkv, hd, kv_cap))
+    return false;
+  *mkt = *mk;
+  *mvt = *mv;
+  return true;
+}
+
 template <int HD, bool BF16>
 static int launch(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int Sq, int Skv,
                   int kv_cap, int causal, float scale, cudaStream_t stream, int dev, const Paged* pg = nullptr) {
@@ -1327,31 +1383,10 @@ static int launch(const void* q, const void* k, const void* v, void* o, int B, i
   EncodeTiledFn enc = encoder();
   if (!enc) return FA_ERR_LAUNCH;
   CUtensorMap mq, mk, mv, mo, mkt, mvt;
-  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, HD, Sq) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, HD, Sq))
-    return FA_ERR_LAUNCH;
-  int last_page = 0;
-  if (pg && Skv > 0) {
-    // whole pages through the pool maps; the last page through maps that end
-    // at its last valid row, so rows past Skv load as zeros
-    last_page = (Skv - 1) / pg->page_size;
-    const int tail_rows = Skv - last_page * pg->page_size;
-    if (!encode_bshd(&mk, enc, k, BF16, pg->num_blocks, pg->page_size, Hkv, HD, pg->page_size) ||
-        !encode_bshd(&mv, enc, v, BF16, pg->num_blocks, pg->page_size, Hkv, HD, pg->page_size) ||
-        !encode_bshd(&mkt, enc, k, BF16, pg->num_blocks, tail_rows, Hkv, HD, pg->page_size) ||
-        !encode_bshd(&mvt, enc, v, BF16, pg->num_blocks, tail_rows, Hkv, HD, pg->page_size))
-      return FA_ERR_LAUNCH;
-  } else {
-    if (!encode_bshd(&mk, enc, k, BF16, B, Skv, Hkv, HD, kv_cap) || !encode_bshd(&mv, enc, v, BF16, B, Skv, Hkv, HD, kv_cap))
-      return FA_ERR_LAUNCH;
-    mkt = mk;
-    mvt = mv;
-  }
   Params prm;
-  prm.block_table = (pg && Skv > 0) ? pg->table : nullptr;
-  prm.page_size = pg ? pg->page_size : 0;
-  prm.max_pages = pg ? pg->max_pages : 0;
-  prm.num_blocks = pg ? pg->num_blocks : 0;
-  prm.last_page = last_page;
+  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, HD, Sq) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, HD, Sq) ||
+      !encode_kv(&mk, &mv, &mkt, &mvt, enc, k, v, BF16, B, Skv, kv_cap, Hkv, HD, pg, &prm))
+    return FA_ERR_LAUNCH;
   prm.o = static_cast<uint16_t*>(o);
   prm.B = B;
   prm.Hq = Hq;
@@ -1556,7 +1591,8 @@ static std::atomic<unsigned> g_seq{0};
 
 template <int HD, bool BF16>
 static int launch_sk(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int Sq, int Skv,
-                     int kv_cap, int causal, float scale, void* ws, cudaStream_t stream, int dev) {
+                     int kv_cap, int causal, float scale, void* ws, cudaStream_t stream, int dev,
+                     const Paged* pg = nullptr) {
   using SL = SkLayout<HD>;
   auto kern = fa_prefill_sk_kernel<HD, BF16>;
   const int slot = (HD == 128 ? 2 : 0) + (BF16 ? 1 : 0);
@@ -1569,9 +1605,10 @@ static int launch_sk(const void* q, const void* k, const void* v, void* o, int B
   }
   EncodeTiledFn enc = encoder();
   if (!enc) return FA_ERR_LAUNCH;
-  CUtensorMap mq, mk, mv, mo;
-  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, HD, Sq) || !encode_bshd(&mk, enc, k, BF16, B, Skv, Hkv, HD, kv_cap) ||
-      !encode_bshd(&mv, enc, v, BF16, B, Skv, Hkv, HD, kv_cap) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, HD, Sq))
+  CUtensorMap mq, mk, mv, mo, mkt, mvt;
+  Params pkv;
+  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, HD, Sq) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, HD, Sq) ||
+      !encode_kv(&mk, &mv, &mkt, &mvt, enc, k, v, BF16, B, Skv, kv_cap, Hkv, HD, pg, &pkv))
     return FA_ERR_LAUNCH;
   SkParams sp;
   std::memset(&sp, 0, sizeof(sp));
@@ -1587,6 +1624,11 @@ static int launch_sk(const void* q, const void* k, const void* v, void* o, int B
   prm.pair_heads = (prm.G % 2 == 0) ? 1 : 0;
   prm.causal = causal ? 1 : 0;
   prm.sl2 = scale * 1.4426950408889634f;
+  prm.block_table = pkv.block_table;
+  prm.page_size = pkv.page_size;
+  prm.max_pages = pkv.max_pages;
+  prm.num_blocks = pkv.num_blocks;
+  prm.last_page = pkv.last_page;
   prm.watchdog_ns = WATCHDOG_NS;
   SkSchedule sc;
   get_schedule(prm, g_dev_sms[dev].load(), &sc);
@@ -1610,7 +1652,7 @@ static int launch_sk(const void* q, const void* k, const void* v, void* o, int B
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, sp) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, mkt, mvt, sp) != cudaSuccess) {
     (void)cudaGetLastError();
     return FA_ERR_LAUNCH;
   }
@@ -1662,7 +1704,7 @@ static int run_kvcache(bool bf16, const void* q, const void* k, const void* v, v
 // Attention over a paged K/V pool (one-shot kernel).
 static int run_paged(bool bf16, const void* q, const void* k_pool, const void* v_pool, const void* block_table,
                      void* o, int B, int Hq, int Hkv, int Sq, int kv_len, int hd, int page_size, int max_pages,
-                     int num_blocks, int causal, float scale, void* stream) {
+                     int num_blocks, int causal, float scale, void* ws, size_t ws_bytes, void* stream) {
   if (kv_len < 0 || page_size < BN || page_size % BN != 0 || max_pages < 0 || num_blocks < 1)
     return FA_ERR_INVALID_ARG;
   if ((long long)max_pages * page_size < kv_len) return FA_ERR_INVALID_ARG;
@@ -1687,6 +1729,15 @@ static int run_paged(bool bf16, const void* q, const void* k_pool, const void* v
   if (ds != FA_OK) return ds;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const Paged pg{static_cast<const int*>(block_table), page_size, max_pages, num_blocks};
+  if (ws) {  // split-KV over the pool
+    if (reinterpret_cast<uintptr_t>(ws) & 255u) return FA_ERR_ALIGNMENT;
+    if (ws_bytes < ws_bytes_for(hd)) return FA_ERR_INVALID_ARG;
+    if (hd == 128)
+      return bf16 ? launch_sk<128, true>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, ws, st, dev, &pg)
+                  : launch_sk<128, false>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, ws, st, dev, &pg);
+    return bf16 ? launch_sk<64, true>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, ws, st, dev, &pg)
+                : launch_sk<64, false>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, ws, st, dev, &pg);
+  }
   if (hd == 128)
     return bf16 ? launch<128, true>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, st, dev, &pg)
                 : launch<128, false>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, st, dev, &pg);
@@ -1826,7 +1877,7 @@ static int launch_sk_static(const void* q, const void* k, const void* v, void* o
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, sp) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, mk, mv, sp) != cudaSuccess) {
     (void)cudaGetLastError();
     return FA_ERR_LAUNCH;
   }
@@ -1892,7 +1943,16 @@ extern "C" int fa_prefill_paged(const void* q, const void* k_pool, const void* v
                                 void* o, int B, int Hq, int Hkv, int Sq, int kv_len, int hd, int page_size,
                                 int max_pages, int num_blocks, int causal, float scale, int bf16, void* stream) {
   return fa::run_paged(bf16 != 0, q, k_pool, v_pool, block_table, o, B, Hq, Hkv, Sq, kv_len, hd, page_size,
-                       max_pages, num_blocks, causal, scale, stream);
+                       max_pages, num_blocks, causal, scale, nullptr, 0, stream);
+}
+
+extern "C" int fa_prefill_paged_ws(const void* q, const void* k_pool, const void* v_pool, const void* block_table,
+                                   void* o, int B, int Hq, int Hkv, int Sq, int kv_len, int hd, int page_size,
+                                   int max_pages, int num_blocks, int causal, float scale, int bf16, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  if (!workspace) return FA_ERR_INVALID_ARG;
+  return fa::run_paged(bf16 != 0, q, k_pool, v_pool, block_table, o, B, Hq, Hkv, Sq, kv_len, hd, page_size,
+                       max_pages, num_blocks, causal, scale, workspace, workspace_bytes, stream);
 }
 
 extern "C" int fa_kv_append(const void* k_new, const void* v_new, const void* positions, void* k_cache, void* v_cache,

@@ -214,6 +214,23 @@ int fa_prefill_paged(const void* q, const void* k_pool, const void* v_pool,
                      void* stream);
 
 /*
+ * fa_prefill_paged_ws -- fa_prefill_paged computed by the split-KV kernel
+ * (fa_prefill_ws's kernel, with the same paged producer): the arguments of
+ * fa_prefill_paged, then a workspace under fa_prefill_ws's rules (caller-owned,
+ * >= fa_workspace_bytes(hd), 256-byte aligned, zero-filled before first use,
+ * not shared by overlapping calls).  For a chunk over a long paged context,
+ * where the one-shot grid leaves most SMs idle (fa_split_kv_advised).
+ * Errors: those of fa_prefill_paged and fa_prefill_ws (NULL, small or
+ * misaligned workspace); hd 64 and 128 only.
+ */
+int fa_prefill_paged_ws(const void* q, const void* k_pool, const void* v_pool,
+                        const void* block_table, void* o, int B, int Hq,
+                        int Hkv, int Sq, int kv_len, int hd, int page_size,
+                        int max_pages, int num_blocks, int causal, float scale,
+                        int bf16, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/*
  * fa_kv_append -- the K/V-cache append before a chunked prefill's attention
  * (the pages' store_kv kernel, minfer "11 · P5 — prefill gap session: TM=128
  * big tiles + FA rewrite", section 3.2), for K and V in one launch:

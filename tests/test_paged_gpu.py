@@ -51,15 +51,21 @@ CASES = [  # (B, Hq, Hkv, Sq, kv_len, hd, dtype, page)
 ]
 
 
+@pytest.fixture(params=[False, True], ids=["oneshot", "streamk"])
+def split(request):
+    return request.param
+
+
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "B{}_H{}-{}_Sq{}_kv{}_hd{}_{}_p{}".format(*c))
-def test_paged_matches_oracle_and_contiguous_path(case):
+def test_paged_matches_oracle_and_contiguous_path(case, split):
     fa = _fa()
     B, Hq, Hkv, Sq, kv_len, hd, dtype, page = case
     w = W.Workload("case", B, Hq, Hkv, Sq, kv_len, hd, dtype=dtype, seed=kv_len + page)
     q, k, v = W.make_inputs(w)
     kp, vp, table = _paged(k, v, page, seed=page)
-    out = fa.attention_paged(q.cuda(), kp.cuda(), vp.cuda(), table.cuda(), kv_len, causal=True, scale=w.scale)
-    ref = fa.attention(q.cuda(), k.cuda(), v.cuda(), causal=True, scale=w.scale, split=False)
+    out = fa.attention_paged(q.cuda(), kp.cuda(), vp.cuda(), table.cuda(), kv_len, causal=True, scale=w.scale,
+                             split=split)
+    ref = fa.attention(q.cuda(), k.cuda(), v.cuda(), causal=True, scale=w.scale, split=split)
     torch.cuda.synchronize()
     assert fa.debug_status() == 0
     assert torch.equal(out, ref)  # same tiles, same kernel: only the load addresses differ
@@ -87,6 +93,29 @@ def test_paged_full_size_gqa_prompt_sampled_rows():
     want = oracle.attention_rows(q, k, v, rows.numpy(), causal=True, scale=w.scale)
     g = out.cpu()[rows[:, 0].long(), rows[:, 2].long(), rows[:, 1].long()].double().numpy()
     assert (np.abs(g - want) / (1 + np.abs(want))).max() <= TOL["bf16"]
+
+
+def test_paged_long_context_chunk_split_kv():
+    """The serving case split-KV exists for: a 128-row chunk over a long paged
+    context (few query tiles, long rows).  Split-KV and one-shot agree with the
+    oracle on sampled rows; split-KV is bit-identical to its contiguous run."""
+    fa = _fa()
+    w = W.Workload("case", 1, 16, 4, 128, 9000, 128, seed=31)
+    q, k, v = W.make_inputs(w)
+    kp, vp, table = _paged(k, v, 256, seed=31)
+    dq, dkp, dvp, dt = q.cuda(), kp.cuda(), vp.cuda(), table.cuda()
+    assert fa.split_kv_advised(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, True)
+    a = fa.attention_paged(dq, dkp, dvp, dt, w.Skv, causal=True, scale=w.scale)             # advised: split-KV
+    b = fa.attention_paged(dq, dkp, dvp, dt, w.Skv, causal=True, scale=w.scale, split=False)
+    c = fa.attention(dq, k.cuda(), v.cuda(), causal=True, scale=w.scale, split=True)
+    torch.cuda.synchronize()
+    assert fa.debug_status() == 0
+    assert torch.equal(a, c)
+    rows = W.sample_rows(w, 256)
+    want = oracle.attention_rows(q, k, v, rows.numpy(), causal=True, scale=w.scale)
+    for got in (a, b):
+        g = got.cpu()[rows[:, 0].long(), rows[:, 2].long(), rows[:, 1].long()].double().numpy()
+        assert (np.abs(g - want) / (1 + np.abs(want))).max() <= TOL["f16"]
 
 
 def test_block_outside_the_pool_is_reported():
