@@ -75,6 +75,9 @@ def _load():
             lib.oracle_round_bf16.restype = ctypes.c_uint16
             lib.oracle_kv_append.argtypes = ([ctypes.c_void_p] * 5 + [i32] * 6)
             lib.oracle_kv_append.restype = ctypes.c_longlong
+            lib.oracle_lse_rows.argtypes = ([d, d] + [i32] * 7 + [ctypes.c_double]
+                                            + [ctypes.POINTER(ctypes.c_int32), ctypes.c_longlong, d])
+            lib.oracle_lse_rows.restype = i32
             _lib = lib
     return _lib
 
@@ -84,7 +87,7 @@ def _load():
 PLANTED_MISTAKES = {
     "none": 0, "no_scale": 1, "top_left": 2, "mask_off_by_one": 3, "gqa_modulo": 4,
     "no_normalise": 5, "v_reversed": 6, "no_max_subtract": 7, "exp2": 8, "masked_row_nan": 9,
-    "round_truncate": 10, "round_ties_away": 11, "append_at_t": 12,
+    "round_truncate": 10, "round_ties_away": 11, "append_at_t": 12, "lse_log2": 13,
 }
 
 
@@ -212,3 +215,30 @@ def gather_pages(pool, block_table, kv_len: int, page_size: int):
     table = np.asarray(block_table.cpu().numpy() if hasattr(block_table, "cpu") else block_table, dtype=np.int64)
     j = np.arange(kv_len)
     return np.ascontiguousarray(pool[table[:, j // page_size], j % page_size])
+
+
+def lse_rows(q, k, rows, causal: bool = True, scale: float | None = None) -> np.ndarray:
+    """Per-row log-sum-exp of the scaled, masked scores for rows [n, 3] =
+    (b, hq, i): log sum_j exp(s_j) over the visible keys, -inf for a row that
+    sees none.  Returns float64 [n]."""
+    qa, ka = _f64(q), _f64(k)
+    B, Sq, Hq, hd = qa.shape
+    _, Skv, Hkv, _ = ka.shape
+    if scale is None:
+        scale = 1.0 / float(np.sqrt(hd))
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 3))
+    out = np.empty(r.shape[0], dtype=np.float64)
+    rc = _load().oracle_lse_rows(_ptr(qa), _ptr(ka), B, Hq, Hkv, Sq, Skv, hd, int(bool(causal)), float(scale),
+                                 r.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), r.shape[0], _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle_lse_rows failed ({rc})")
+    return out
+
+
+def lse(q, k, causal: bool = True, scale: float | None = None) -> np.ndarray:
+    """log-sum-exp of every row, as [B, Hq, Sq] float64."""
+    qa = _f64(q)
+    B, Sq, Hq, _ = qa.shape
+    bb, hh, ii = np.meshgrid(np.arange(B), np.arange(Hq), np.arange(Sq), indexing="ij")
+    rows = np.stack([bb.ravel(), hh.ravel(), ii.ravel()], axis=1)
+    return lse_rows(q, k, rows, causal, scale).reshape(B, Hq, Sq)

@@ -64,7 +64,8 @@ enum {
     PLANT_ROUND_TRUNCATE = 10, /* cache append rounds toward zero           */
     PLANT_ROUND_TIES_AWAY = 11,/* cache append breaks ties away from zero   */
     PLANT_APPEND_AT_T = 12,    /* cache append writes row t, not positions[t] */
-    PLANT_COUNT = 13
+    PLANT_LSE_LOG2 = 13,       /* log-sum-exp taken in base 2               */
+    PLANT_COUNT = 14
 };
 static int g_plant = PLANT_NONE;
 
@@ -273,6 +274,45 @@ int oracle_probs_row(const double *q, const double *k,
     return ORACLE_OK;
 }
 
+
+/* ------------------------------------------------------------------------
+ * Per-row log-sum-exp (the natural log of the softmax denominator), the
+ * quantity split-KV pieces are combined by -- the pages' running max m and
+ * sum l of the online softmax (minfer "53 · r50 — FA_TKV 32->16 occupancy
+ * experiment", section 2) taken together: lse = m + log(l):
+ *
+ *   lse = log sum_j exp(s_j)   over the visible keys j (s_j scaled, masked)
+ *   lse = -inf                  when the row sees no key
+ *
+ * computed as m + log(sum_j exp(s_j - m)) from the same score row as the
+ * attention.  rows: [n][3] = (b, hq, i).
+ */
+int oracle_lse_rows(const double *q, const double *k, int B, int Hq, int Hkv, int Sq, int Skv, int hd,
+                    int causal, double scale, const int32_t *rows, long long n, double *lse)
+{
+    shape_t s = {q, k, k, B, Hq, Hkv, Sq, Skv, hd, causal, scale}; /* v is not read */
+    if (!lse || (n > 0 && !rows) || check_shape(&s) != ORACLE_OK) return ORACLE_BAD_ARG;
+    double *srow = (double *)malloc(sizeof(double) * (size_t)(Skv > 0 ? Skv : 1));
+    if (!srow) return ORACLE_NO_MEMORY;
+    for (long long r = 0; r < n; ++r) {
+        const int b = rows[3 * r], hq = rows[3 * r + 1], i = rows[3 * r + 2];
+        if (b < 0 || b >= B || hq < 0 || hq >= Hq || i < 0 || i >= Sq) {
+            free(srow);
+            return ORACLE_BAD_ARG;
+        }
+        const double m = score_row(&s, b, hq, i, srow);
+        if (m == -INFINITY) {
+            lse[r] = -INFINITY;
+            continue;
+        }
+        double sum = 0.0;
+        for (int j = 0; j < Skv; ++j)
+            if (srow[j] != -INFINITY) sum += exp(srow[j] - m);
+        lse[r] = m + ((g_plant == PLANT_LSE_LOG2) ? log2(sum) : log(sum));
+    }
+    free(srow);
+    return ORACLE_OK;
+}
 
 /* ------------------------------------------------------------------------
  * K/V-cache append (the step before a chunked prefill's attention: the pages'

@@ -419,6 +419,38 @@ def test_kv_append_scatters_rounded_rows_to_positions():
         assert np.array_equal(kc, wk) and np.array_equal(vc, wv)
 
 
+def test_lse_by_brute_force_and_closed_forms():
+    """The per-row log-sum-exp: exact on tiny integer inputs (50-digit decimal
+    exp and ln of the visible scores), log(n) + s for n identical visible
+    scores, s_0 for a row that sees one key, -inf for a row that sees none."""
+    getcontext().prec = 50
+    rng = np.random.default_rng(12)
+    B, Hq, Hkv, Sq, Skv, hd = 1, 2, 1, 3, 5, 4
+    q = rng.integers(-3, 4, size=(B, Sq, Hq, hd)).astype(np.float64)
+    k = rng.integers(-3, 4, size=(B, Skv, Hkv, hd)).astype(np.float64)
+    scale = 0.25
+    got = oracle.lse(q, k, causal=True, scale=scale)
+    off = Skv - Sq
+    for hq in range(Hq):
+        for i in range(Sq):
+            tot = Decimal(0)
+            for j in range(off + i + 1):
+                sc = Decimal(scale) * Decimal(int(np.dot(q[0, i, hq], k[0, j, 0])))
+                tot += sc.exp()
+            assert abs(float(tot.ln()) - got[0, hq, i]) < 1e-12
+    # identical keys: row i sees n = off + i + 1 equal scores s
+    k2 = np.repeat(k[:, :1], Skv, axis=1)
+    got2 = oracle.lse(q, k2, causal=True, scale=scale)
+    for hq in range(Hq):
+        for i in range(Sq):
+            s0 = scale * float(np.dot(q[0, i, hq], k2[0, 0, 0]))
+            assert abs(got2[0, hq, i] - (s0 + math.log(off + i + 1))) < 1e-12
+    # Sq > Skv: the first rows see nothing; the first row that sees one key gives s_0
+    got3 = oracle.lse(q[:, :3], k[:, :2], causal=True, scale=scale)
+    assert np.isneginf(got3[0, :, 0]).all() and np.isfinite(got3[0, :, 1:]).all()
+    assert abs(got3[0, 0, 1] - scale * float(np.dot(q[0, 1, 0], k[0, 0, 0]))) < 1e-12
+
+
 def test_gather_pages_by_brute_force():
     """The paged-cache gather against a loop over every key: key j of sequence
     b is row j % page of block table[b][j // page]."""
@@ -459,6 +491,7 @@ def _pin_battery():
         ("round_bf16", test_round_bf16_matches_ieee_conversion),
         ("round_ties", test_round_ties_go_to_even),
         ("kv_append", test_kv_append_scatters_rounded_rows_to_positions),
+        ("lse", test_lse_by_brute_force_and_closed_forms),
     ]
 
 
