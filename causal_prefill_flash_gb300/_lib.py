@@ -34,6 +34,7 @@ _SIG = {
                                 _P]),
     "fa_workspace_bytes": (ctypes.c_size_t, [_I]),
     "fa_split_kv_advised": (_I, [_I, _I, _I, _I, _I, _I]),
+    "fa_prefill_ex": (_I, [_P, _P, _P, _P, _P] + [_I] * 7 + [ctypes.c_float, _I, _P, ctypes.c_size_t, _P]),
     "fa_prefill_kvcache": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _I, _P,
                                 ctypes.c_size_t, _P]),
     "fa_kv_append": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
@@ -275,6 +276,14 @@ def attention_kvcache(q, k_cache, v_cache, kv_len: int, causal: bool = True, sca
     return out
 
 
+def fa_prefill_ex(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, hd, causal, scale, bf16, workspace=None,
+                  workspace_bytes=0, stream=None) -> int:
+    """Any hd, either kernel, optional log-sum-exp: the C function's arguments. Returns the status."""
+    return int(load().fa_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(Hq), int(Hkv),
+                                    int(Sq), int(Skv), int(hd), int(causal), float(scale), int(bf16),
+                                    _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
 def split_kv_advised(B, Hq, Hkv, Sq, Skv, causal=True) -> bool:
     """The library's advice for this shape on the current device: True when the
     split-KV kernel is expected to beat the one-shot kernel."""
@@ -304,7 +313,7 @@ def workspace_for(device, hd: int, stream=None):
 
 
 def attention(q, k, v, causal: bool = True, scale: float | None = None, out=None, stream=None,
-              split: bool | None = None):
+              split: bool | None = None, return_lse: bool = False):
     """O = softmax(scale Q K^T + causal mask) V for BSHD CUDA tensors.
 
     q: [B, Sq, Hq, hd], k/v: [B, Skv, Hkv, hd], all float16 or all bfloat16,
@@ -312,7 +321,9 @@ def attention(q, k, v, causal: bool = True, scale: float | None = None, out=None
     (written into ``out`` when given).  ``split=True`` uses the load-balanced
     stream-K (split-KV) kernel with a cached workspace, ``split=False`` the
     one-shot kernel, ``split=None`` whichever the library advises for the
-    shape (``split_kv_advised``).  Raises FaError on any library error.
+    shape (``split_kv_advised``).  ``return_lse=True`` also returns the
+    per-row log-sum-exp of the scaled scores, float32 [B, Hq, Sq] (-inf for a
+    row that sees no key).  Raises FaError on any library error.
     """
     import torch
     if not (q.is_cuda and k.is_cuda and v.is_cuda):
@@ -335,6 +346,14 @@ def attention(q, k, v, causal: bool = True, scale: float | None = None, out=None
         raise ValueError("out must be a contiguous CUDA tensor like q")
     if split is None:  # split-KV exists for hd 64 and 128
         split = hd != 256 and split_kv_advised(B, Hq, Hkv, Sq, Skv, causal)
+    if return_lse:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+        ws = workspace_for(q.device, hd, stream) if split else None
+        st = fa_prefill_ex(q, k, v, out, lse, B, Hq, Hkv, Sq, Skv, hd, int(bool(causal)), scale,
+                           int(q.dtype == torch.bfloat16), ws, ws.numel() if ws is not None else 0, stream)
+        if st != FA_OK:
+            raise FaError(st, "fa_prefill_ex")
+        return out, lse
     if split:
         fn = fa_prefill_ws_bf16 if q.dtype == torch.bfloat16 else fa_prefill_ws
         ws = workspace_for(q.device, hd, stream)

@@ -139,7 +139,14 @@ struct Params {
   // (t * BN) % page_size; the last page is read through the tail maps
   const int* block_table;  // nullptr: contiguous [B][Skv][Hkv][hd] K/V
   int page_size, max_pages, num_blocks, last_page;
+  float* lse;  // nullptr, or [B][Hq][Sq]: log sum_j exp(scale s_j) of every row (-inf: no key)
 };
+
+// A row's log-sum-exp from the online-softmax state: m (log2 units of
+// scale * log2(e) * s) and l = sum 2^(s' - m), so lse = (m + log2 l) ln 2.
+__device__ __forceinline__ float row_lse(float m, float l) {
+  return l > 0.f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+}
 
 // The two query tiles of one CTA.  Longest tiles first; for head pairs the
 // G/2 CTAs of one KV group are adjacent so their K/V tiles come from L2.
@@ -555,6 +562,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (ok) ptx::tc_fence_after();
     }
     if (ok && hasx) {
+      if (p.lse && q0 + r < p.Sq) p.lse[(static_cast<size_t>(w.b) * p.Hq + hqx) * p.Sq + q0 + r] = row_lse(m_ref, l);
       // O / l rounded to 16 bits, written 128-byte swizzled (the layout of a Q
       // tile) and sent out by TMA tensor stores, one per 64-column block: the
       // global writes are whole lines, and rows past Sq are clipped by the map.
@@ -1126,6 +1134,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       // KV tile 0 is here: this CTA writes the output, merging the later pieces
       // (CTAs cta+1, cta+2, ... whose ranges start inside this pair) in order
+      // (a pair held whole has none: kend stays cta + 1)
       float M = ntile > 0 ? m_ref : -INFINITY;
       int kend = cta + 1;
       if (!last) {
@@ -1161,6 +1170,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (mk_ != -INFINITY) Lsum += lk * ptx::ex2(mk_ - M);
       }
       const float inv_l = (Lsum > 0.f) ? 1.f / Lsum : 0.f;
+      if (p.lse && q0 + r < p.Sq) p.lse[(static_cast<size_t>(w.b) * p.Hq + hqx) * p.Sq + q0 + r] = row_lse(M, Lsum);
 #pragma unroll
       for (int cb = 0; cb < (int)L::KCH; ++cb) {
         ok = stage_wait_free();
@@ -1369,7 +1379,8 @@ static bool encode_kv(CUtensorMap* mk, CUtensorMap* mv, CUtensorMap* mkt, CUtens
 
 template <int HD, bool BF16>
 static int launch(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int Sq, int Skv,
-                  int kv_cap, int causal, float scale, cudaStream_t stream, int dev, const Paged* pg = nullptr) {
+                  int kv_cap, int causal, float scale, cudaStream_t stream, int dev, const Paged* pg = nullptr,
+                  float* lse = nullptr) {
   using L = Layout<HD>;
   auto kern = fa_prefill_kernel<HD, BF16>;
   const int slot = (HD == 128 ? 2 : 0) + (BF16 ? 1 : 0);
@@ -1387,6 +1398,7 @@ static int launch(const void* q, const void* k, const void* v, void* o, int B, i
   if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, HD, Sq) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, HD, Sq) ||
       !encode_kv(&mk, &mv, &mkt, &mvt, enc, k, v, BF16, B, Skv, kv_cap, Hkv, HD, pg, &prm))
     return FA_ERR_LAUNCH;
+  prm.lse = lse;
   prm.o = static_cast<uint16_t*>(o);
   prm.B = B;
   prm.Hq = Hq;
@@ -1411,7 +1423,7 @@ static int launch(const void* q, const void* k, const void* v, void* o, int B, i
 // hd = 256: one query tile per CTA (fa_prefill256_kernel).
 template <bool BF16>
 static int launch256(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int Sq, int Skv,
-                     int kv_cap, int causal, float scale, cudaStream_t stream, int dev) {
+                     int kv_cap, int causal, float scale, cudaStream_t stream, int dev, float* lse = nullptr) {
   using L = Layout256;
   auto kern = fa_prefill256_kernel<BF16>;
   if (g_attr256_set[dev][BF16 ? 1 : 0].load() == 0) {
@@ -1440,6 +1452,7 @@ static int launch256(const void* q, const void* k, const void* v, void* o, int B
   prm.causal = causal ? 1 : 0;
   prm.sl2 = scale * 1.4426950408889634f;
   prm.watchdog_ns = WATCHDOG_NS;
+  prm.lse = lse;
   const long long grid = (long long)prm.n_qtiles * Hq * B;
   if (grid > 0x7FFFFFFFLL) return FA_ERR_UNSUPPORTED;
   if (launch_pdl(kern, dim3((unsigned)grid), dim3(NUM_THREADS_256), L::REQUEST, stream, mq, mk, mv, mo, prm) !=
@@ -1592,7 +1605,7 @@ static std::atomic<unsigned> g_seq{0};
 template <int HD, bool BF16>
 static int launch_sk(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int Sq, int Skv,
                      int kv_cap, int causal, float scale, void* ws, cudaStream_t stream, int dev,
-                     const Paged* pg = nullptr) {
+                     const Paged* pg = nullptr, float* lse = nullptr) {
   using SL = SkLayout<HD>;
   auto kern = fa_prefill_sk_kernel<HD, BF16>;
   const int slot = (HD == 128 ? 2 : 0) + (BF16 ? 1 : 0);
@@ -1629,6 +1642,7 @@ static int launch_sk(const void* q, const void* k, const void* v, void* o, int B
   prm.max_pages = pkv.max_pages;
   prm.num_blocks = pkv.num_blocks;
   prm.last_page = pkv.last_page;
+  prm.lse = lse;
   prm.watchdog_ns = WATCHDOG_NS;
   SkSchedule sc;
   get_schedule(prm, g_dev_sms[dev].load(), &sc);
@@ -1743,6 +1757,46 @@ static int run_paged(bool bf16, const void* q, const void* k_pool, const void* v
                 : launch<128, false>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, st, dev, &pg);
   return bf16 ? launch<64, true>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, st, dev, &pg)
               : launch<64, false>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, st, dev, &pg);
+}
+
+// Any supported hd, either kernel (a workspace selects split-KV), and an
+// optional per-row log-sum-exp output.
+static int run_ex(bool bf16, const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                  int Hkv, int Sq, int Skv, int hd, int causal, float scale, void* ws, size_t ws_bytes, void* stream) {
+  bool empty = false;
+  const int vs = validate(q, k, v, o, B, Hq, Hkv, Sq, Skv, hd, scale, &empty);
+  if (vs != FA_OK || empty) return vs;
+  if (lse) {
+    if (reinterpret_cast<uintptr_t>(lse) & 3u) return FA_ERR_ALIGNMENT;
+    const size_t ln = (size_t)B * Hq * Sq * 4, qn = (size_t)B * Sq * Hq * hd * 2, kn = (size_t)B * Skv * Hkv * hd * 2;
+    if (overlaps(lse, ln, q, qn) || overlaps(lse, ln, o, qn) || (Skv > 0 && (overlaps(lse, ln, k, kn) || overlaps(lse, ln, v, kn))))
+      return FA_ERR_INVALID_ARG;
+  }
+  if (ws) {
+    if (hd == 256) return FA_ERR_UNSUPPORTED;
+    if (reinterpret_cast<uintptr_t>(ws) & 255u) return FA_ERR_ALIGNMENT;
+    if (ws_bytes < ws_bytes_for(hd)) return FA_ERR_INVALID_ARG;
+    if (lse && overlaps(lse, (size_t)B * Hq * Sq * 4, ws, ws_bytes)) return FA_ERR_INVALID_ARG;
+  }
+  int dev = -1;
+  const int ds = check_device(&dev);
+  if (ds != FA_OK) return ds;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (hd == 256)
+    return bf16 ? launch256<true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev, lse)
+                : launch256<false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev, lse);
+  if (ws) {
+    if (hd == 128)
+      return bf16 ? launch_sk<128, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, ws, st, dev, nullptr, lse)
+                  : launch_sk<128, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, ws, st, dev, nullptr, lse);
+    return bf16 ? launch_sk<64, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, ws, st, dev, nullptr, lse)
+                : launch_sk<64, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, ws, st, dev, nullptr, lse);
+  }
+  if (hd == 128)
+    return bf16 ? launch<128, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev, nullptr, lse)
+                : launch<128, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev, nullptr, lse);
+  return bf16 ? launch<64, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev, nullptr, lse)
+              : launch<64, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev, nullptr, lse);
 }
 
 static int run_ws(bool bf16, const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int Sq,
@@ -1958,6 +2012,13 @@ extern "C" int fa_prefill_paged_ws(const void* q, const void* k_pool, const void
 extern "C" int fa_kv_append(const void* k_new, const void* v_new, const void* positions, void* k_cache, void* v_cache,
                             int B, int T, int Hkv, int hd, int kv_cap, int bf16, void* stream) {
   return fa::run_kv_append(k_new, v_new, positions, k_cache, v_cache, B, T, Hkv, hd, kv_cap, bf16 != 0, stream);
+}
+
+extern "C" int fa_prefill_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                             int Hkv, int Sq, int Skv, int hd, int causal, float scale, int bf16, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  return fa::run_ex(bf16 != 0, q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, hd, causal, scale, workspace, workspace_bytes,
+                    stream);
 }
 
 extern "C" int fa_split_kv_advised(int B, int Hq, int Hkv, int Sq, int Skv, int causal) {

@@ -340,6 +340,7 @@ __global__ void __launch_bounds__(NUM_THREADS_256, 1)
       if (ok) ptx::tc_fence_after();
     }
     if (ok) {
+      if (p.lse && q0 + r < p.Sq) p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.Sq + q0 + r] = row_lse(m_ref, l);
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
       const uint32_t stage = sRing + r * 128;
 #pragma unroll 1

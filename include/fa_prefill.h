@@ -147,6 +147,28 @@ int fa_prefill_ws_bf16(const void* q, const void* k, const void* v, void* o,
 size_t fa_workspace_bytes(int hd);
 
 /*
+ * fa_prefill_ex -- one entry point for every head dimension and both kernels,
+ * with an optional per-row log-sum-exp output:
+ *   q, k, v, o, B ... scale   as fa_prefill
+ *   lse        NULL, or DEVICE float [B][Hq][Sq], 4-byte aligned, written:
+ *              lse[b][hq][i] = log sum_j exp(scale * q_i . k_j) over the keys
+ *              row i sees (-inf for a row that sees none) -- the online
+ *              softmax's running max and sum taken together (minfer "53 · r50
+ *              — FA_TKV 32->16 occupancy experiment", section 2), which is
+ *              what combines attention computed over separate key ranges
+ *   bf16       0: f16, non-zero: bfloat16
+ *   workspace  NULL: the one-shot kernel (hd 64, 128 or 256); otherwise the
+ *              split-KV kernel under fa_prefill_ws's rules (hd 64 and 128)
+ * Errors: those of fa_prefill / fa_prefill_ws, FA_ERR_ALIGNMENT for a
+ * misaligned lse, FA_ERR_INVALID_ARG for lse overlapping q, k, v, o or the
+ * workspace.
+ */
+int fa_prefill_ex(const void* q, const void* k, const void* v, void* o,
+                  float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int hd,
+                  int causal, float scale, int bf16, void* workspace,
+                  size_t workspace_bytes, void* stream);
+
+/*
  * fa_split_kv_advised -- host-only advice on which kernel to call for a shape
  * on the current device: 1 if fa_prefill_ws (split-KV) is expected to be
  * faster than fa_prefill, 0 if not, a negative fa_status_t on error (-1 bad

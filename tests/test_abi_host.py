@@ -182,3 +182,13 @@ def test_paged_errors_without_a_device(fa):
     assert call(bt=24 * A + 2) == 3 and call(hd=96) == 2
     assert call(o=9 * A) == 1                     # o inside the K pool
     assert call(B=0) == 0
+
+
+def test_ex_entry_point_errors_without_a_device(fa):
+    f = fa.fa_prefill_ex
+    args = (A, 2 * A, 3 * A, 4 * A)
+    assert f(*args, 5 * A + 2, 1, 4, 2, 8, 8, 128, 1, 0.1, 0, 0, 0, 0) == 3       # misaligned lse
+    assert f(*args, 4 * A, 1, 4, 2, 8, 8, 128, 1, 0.1, 0, 0, 0, 0) == 1           # lse inside o
+    assert f(*args, 0, 1, 4, 2, 8, 8, 96, 1, 0.1, 0, 0, 0, 0) == 2
+    assert f(*args, 0, 1, 4, 2, 8, 8, 256, 1, 0.1, 0, 6 * A, 1 << 30, 0) == 2     # split-KV: hd 64 and 128
+    assert f(*args, 0, 0, 4, 2, 8, 8, 128, 1, 0.1, 0, 0, 0, 0) == 0               # B = 0
