@@ -59,6 +59,19 @@
  * Errors are returned, never printed and ignored: every entry point returns
  * FA_OK (0) or one of the fa_status_t codes below, and on any error no kernel
  * was launched.
+ *
+ * Entry points
+ * ------------
+ *   fa_prefill, fa_prefill_bf16      one-shot kernel (hd 64, 128, 256)
+ *   fa_prefill_ws, fa_prefill_ws_bf16  split-KV kernel with a caller workspace
+ *   fa_workspace_bytes               its workspace size
+ *   fa_split_kv_advised              which of the two kernels to use for a shape
+ *   fa_prefill_ex                    either kernel, any hd, optional log-sum-exp
+ *   fa_prefill_kvcache               attention over a K/V cache of capacity kv_cap
+ *   fa_prefill_paged, fa_prefill_paged_ws  attention over a paged K/V pool
+ *   fa_kv_append                     write new tokens' K/V rows into a cache
+ *   fa_prefill_ws_static             split-KV with library-owned scratch
+ *   fa_status_string, fa_smem_bytes, fa_debug_status(_clear)  diagnostics
  */
 #ifndef FA_PREFILL_H
 #define FA_PREFILL_H
