@@ -31,6 +31,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 L2_BYTES = 129 * 1024 * 1024
+REFERENCE_SECONDS = 90.0  # the whole reference arm (warmup + steps), whatever K and W
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DEFAULT_WORKLOAD = "prefill7b_s2048"
 
@@ -240,20 +241,49 @@ def oracle_sample(w, seconds: float, seed: int = 4321):
 # ------------------------------------------------------------------- main
 
 def run_reference(args):
+    """The reference arm: the f64 oracle on the host cores, timed on a bounded
+    random sample of output rows per step.  The whole warmup + steps run fits
+    a fixed budget (REFERENCE_SECONDS) whatever K and W are: the oracle's row
+    rate is measured once and each step gets the rows its share of the budget
+    allows (at least one)."""
+    import numpy as np
+
+    import oracle
+    from causal_prefill_flash_gb300 import workloads as W
+
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    from causal_prefill_flash_gb300 import workloads as W
     w = W.get(args.workload)
-    # each step: a bounded sample, sized so warmup + steps end within minutes
-    per_step = max(0.5, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
+    q, k, v = W.make_inputs(w)
+    q64, k64, v64 = (t.double().numpy() for t in (q, k, v))
+    cores = oracle.default_threads()
+    off = w.Skv - w.Sq
+    total_steps = max(1, args.steps + args.warmup)
+
+    def flops_of(rows):
+        return sum(4 * w.hd * max(0, (min(w.Skv, off + int(i) + 1) if w.causal else w.Skv)) for (_, _, i) in rows)
+
+    def run_rows(n, seed):
+        rows = W.sample_rows(w, n, seed=seed).numpy()
+        t0 = time.perf_counter()
+        oracle.attention_rows(q64, k64, v64, rows, causal=w.causal, scale=w.scale, nthreads=cores)
+        return flops_of(rows), time.perf_counter() - t0
+
+    # calibrate: rows per second at the workload's row length
+    fl, dt = run_rows(4 * cores, seed=7)
+    rate = 4 * cores / max(dt, 1e-6)
+    per_step = REFERENCE_SECONDS / total_steps
+    n = max(1, int(rate * per_step))
     vals = []
-    for i in range(args.warmup + args.steps):
-        tf, cores, desc, dt = oracle_sample(w, per_step, seed=1000 + i)
+    for i in range(total_steps):
+        fl, dt = run_rows(n, seed=1000 + i)
         if i >= args.warmup:
-            vals.append((tf, dt))
-    value = statistics.median(v for v, _ in vals)
-    ms = statistics.median(w.flops() / (v * 1e12) * 1e3 for v, _ in vals)
+            vals.append(fl / dt / 1e12)
+    value = statistics.median(vals)
+    ms = w.flops() / (value * 1e12) * 1e3
+    desc = (f"{n} random output rows (b, head, query) of {w.name} per step, each over its full "
+            f"{w.Skv}-key score row, f64, {cores} threads")
     line = {
         "impl": "reference",
         "metric": "causal prefill attention TFLOPS (ms/call, % of dense peak)",
