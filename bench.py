@@ -359,7 +359,7 @@ def run_ours(args):
                 raise fa.FaError(st, "fa_prefill_paged")
     elif split:
         fn = fa.fa_prefill_ws_bf16 if w.dtype == "bf16" else fa.fa_prefill_ws
-        ws = torch.zeros(fa.workspace_bytes(w.hd), dtype=torch.uint8, device=dev)  # zero-filled once
+        ws = torch.empty(fa.workspace_bytes(w.hd), dtype=torch.uint8, device=dev)  # needs no initialisation
         extra = (ws, ws.numel())
     else:
         fn = fa.fa_prefill_bf16 if w.dtype == "bf16" else fa.fa_prefill

@@ -301,13 +301,14 @@ _workspaces = {}
 
 
 def workspace_for(device, hd: int, stream=None):
-    """A zero-filled workspace for the stream-K path, one per (device, stream, hd),
-    allocated once by torch and reused (calls on one stream never overlap)."""
+    """A workspace for the stream-K path, one per (device, stream, hd), allocated
+    once by torch and reused (calls on one stream never overlap; the kernels
+    read only what the same call wrote, so it needs no initialisation)."""
     import torch
     key = (str(device), int(_stream(stream)) if stream is not None else None, int(hd))
     ws = _workspaces.get(key)
     if ws is None:
-        ws = torch.zeros(workspace_bytes(hd), dtype=torch.uint8, device=device)
+        ws = torch.empty(workspace_bytes(hd), dtype=torch.uint8, device=device)
         _workspaces[key] = ws
     return ws
 

@@ -96,7 +96,7 @@ enum : uint32_t {
   WD_SOFTMAX_S_FULL = 7,
   WD_SOFTMAX_O_DONE = 8,
   WD_DRAIN = 9,
-  WD_MERGE_FLAG = 12,
+  WD_PIECE_SLOT = 12,  // a split piece without a workspace slot (inconsistent schedule)
   WD_PAGE_BLOCK = 33,  // a block-table entry outside the pool (its tiles load as zeros)
 };
 
@@ -627,12 +627,11 @@ namespace fa {
 // per CTA.  This kernel runs one persistent CTA per SM and cuts the whole
 // iteration space -- (query-tile pair, KV tile) steps, pairs longest first --
 // into equal contiguous ranges, one per CTA.  A pair whose steps straddle a
-// range boundary is computed in pieces: every piece after the first leaves
-// its unnormalised O, running max m and sum l in the caller's workspace and
-// raises a per-warp flag; the CTA holding the first piece (KV tile 0) waits
-// for those flags and merges the pieces in a fixed order, so results are
-// deterministic.  All CTAs of the grid are co-resident (cooperative launch),
-// and every flag wait is bounded by the watchdog.
+// range boundary is computed in pieces: every piece leaves its unnormalised
+// O, running max m and sum l in a workspace slot the host assigned, and a
+// second, short kernel (fa_sk_merge_kernel, chained by programmatic
+// dependent launch) combines each split pair's pieces over the whole GPU in a
+// fixed order, so results are deterministic.  No CTA waits on another.
 
 constexpr int SK_MAX_CTAS = 256;
 // The persistent loop keeps more state in the control warps than the
@@ -642,14 +641,18 @@ constexpr uint32_t SK_REGS_CONTROL = 88;
 static_assert(128 * SK_REGS_CONTROL + 256 * SK_REGS_SOFTMAX <= NUM_THREADS * LAUNCH_REGS,
               "register split exceeds the launch allocation");
 
+// Workspace slots of split pieces: a CTA holds at most two (the tail of the
+// pair its range starts in, the head of the pair its range ends in).
+constexpr int SK_SLOTS = 2 * SK_MAX_CTAS;
+
 struct SkParams {
   Params p;
-  float4* ws_o;       // partial O, float4 [SK slot][tile][HD/4][BM]
-  float* ws_ml;       // [SK slot][tile][2][BM]: m (log2 domain), l
-  unsigned* ws_flag;  // [SK slot][tile][4 warps]: == seq once that warp's rows are written
-  unsigned seq;       // this launch's sequence number (never 0)
+  float4* ws_o;  // partial O, float4 [piece slot][tile][HD/4][BM]
+  float* ws_ml;  // [piece slot][tile][2][BM]: m (log2 domain), l
   int su[SK_MAX_CTAS + 1];  // CTA c starts at pair unit su[c], KV step sj[c]; it ends where CTA c+1 starts
   int sj[SK_MAX_CTAS + 1];
+  short pf[SK_MAX_CTAS];  // slot of CTA c's first segment when it continues a split pair, else -1
+  short ph[SK_MAX_CTAS];  // slot of CTA c's last segment when it starts a split pair, else -1
 };
 
 template <int HD>
@@ -669,10 +672,9 @@ struct SkLayout {
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr uint32_t BYTES = OFF_MISC + 16;
   static constexpr uint32_t REQUEST = BYTES + 1024;
-  static constexpr size_t WS_O_BYTES = (size_t)SK_MAX_CTAS * 2 * BM * HD * 4;
-  static constexpr size_t WS_ML_BYTES = (size_t)SK_MAX_CTAS * 2 * 2 * BM * 4;
-  static constexpr size_t WS_FLAG_BYTES = (size_t)SK_MAX_CTAS * 2 * 4 * 4;
-  static constexpr size_t WS_BYTES = WS_O_BYTES + WS_ML_BYTES + ((WS_FLAG_BYTES + 255) / 256) * 256;
+  static constexpr size_t WS_O_BYTES = (size_t)SK_SLOTS * 2 * BM * HD * 4;
+  static constexpr size_t WS_ML_BYTES = (size_t)SK_SLOTS * 2 * 2 * BM * 4;
+  static constexpr size_t WS_BYTES = WS_O_BYTES + WS_ML_BYTES;
 };
 
 // Geometry of pair unit u (same numbering as the one-shot grid: longest
@@ -790,6 +792,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = misc[0];
+  // as in the one-shot kernel: set-up overlaps the previous kernel; no global
+  // access before it has completed.  The merge kernel may launch early too.
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
 
   if (warp >= MMA_WARP) {
     ptx::setmaxnreg_dec<SK_REGS_CONTROL>();
@@ -1109,9 +1115,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::tc_fence_after();
       }
       if (!hasx) continue;
-      const size_t slot_t = static_cast<size_t>(cta) * 2 + x;  // this CTA's workspace slot, tile x
-      if (!first) {
-        // a later piece of this pair: leave (O, m, l) for the CTA holding KV tile 0
+      if (!(first && last)) {
+        // a piece of a split pair: (O, m, l) to its slot; the merge kernel
+        // writes the pair's output
+        const int ps = first ? sp.ph[cta] : sp.pf[cta];
+        if (ps < 0) {
+          const uint32_t ci = blockIdx.x < 0xFFFFFFu ? blockIdx.x : 0xFFFFFFu;
+          atomicCAS(&g_fa_status, 0u, WD_PIECE_SLOT | (ci << 8));
+          continue;
+        }
+        const size_t slot_t = static_cast<size_t>(ps) * 2 + x;
         if (ntile > 0) {
           float4* dst = sp.ws_o + slot_t * (HD / 4) * BM + r;
 #pragma unroll
@@ -1128,47 +1141,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         sp.ws_ml[(slot_t * 2 + 0) * BM + r] = ntile > 0 ? m_ref : -INFINITY;
         sp.ws_ml[(slot_t * 2 + 1) * BM + r] = ntile > 0 ? l : 0.f;
-        __syncwarp();
-        if (lane == 0) ptx::st_release_gpu(sp.ws_flag + slot_t * 4 + wq, sp.seq);
         continue;
       }
-      // KV tile 0 is here: this CTA writes the output, merging the later pieces
-      // (CTAs cta+1, cta+2, ... whose ranges start inside this pair) in order
-      // (a pair held whole has none: kend stays cta + 1)
-      float M = ntile > 0 ? m_ref : -INFINITY;
-      int kend = cta + 1;
-      if (!last) {
-        while (kend < static_cast<int>(gridDim.x) && sp.su[kend] == u) ++kend;
-        for (int k = cta + 1; ok && k < kend; ++k) {
-          const unsigned* f = sp.ws_flag + (static_cast<size_t>(k) * 2 + x) * 4 + wq;
-          bool got = ptx::ld_acquire_gpu(f) == sp.seq;
-          if (!got) {
-            const uint64_t t0 = ptx::globaltimer_ns();
-            while (!got) {
-              __nanosleep(128);
-              got = ptx::ld_acquire_gpu(f) == sp.seq;
-              if (!got && (*abort_flag || ptx::globaltimer_ns() - t0 > p.watchdog_ns)) {
-                if (!*abort_flag) {
-                  *abort_flag = 1u;
-                  const uint32_t ci = blockIdx.x < 0xFFFFFFu ? blockIdx.x : 0xFFFFFFu;
-                  atomicCAS(&g_fa_status, 0u, (WD_MERGE_FLAG & 0xFFu) | (ci << 8));
-                }
-                break;
-              }
-            }
-          }
-          ok = __all_sync(0xffffffffu, got);
-          if (ok) M = fmaxf(M, sp.ws_ml[((static_cast<size_t>(k) * 2 + x) * 2 + 0) * BM + r]);
-        }
-        if (!ok) break;
-      }
-      const float fs = (ntile > 0 && m_ref != -INFINITY) ? ptx::ex2(m_ref - M) : 0.f;
-      float Lsum = (ntile > 0) ? l * fs : 0.f;
-      for (int k = cta + 1; k < kend; ++k) {
-        const float mk_ = sp.ws_ml[((static_cast<size_t>(k) * 2 + x) * 2 + 0) * BM + r];
-        const float lk = sp.ws_ml[((static_cast<size_t>(k) * 2 + x) * 2 + 1) * BM + r];
-        if (mk_ != -INFINITY) Lsum += lk * ptx::ex2(mk_ - M);
-      }
+      // a whole pair: O / l straight out
+      const float M = ntile > 0 ? m_ref : -INFINITY;
+      const float Lsum = ntile > 0 ? l : 0.f;
       const float inv_l = (Lsum > 0.f) ? 1.f / Lsum : 0.f;
       if (p.lse && q0 + r < p.Sq) p.lse[(static_cast<size_t>(w.b) * p.Hq + hqx) * p.Sq + q0 + r] = row_lse(M, Lsum);
 #pragma unroll
@@ -1185,24 +1162,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::tmem_wait_ld();
             ptx::reg_fence(orr);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(orr[e]) * fs;
+            for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(orr[e]);
           } else {
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = 0.f;
-          }
-          for (int k = cta + 1; k < kend; ++k) {
-            const float mk_ = sp.ws_ml[((static_cast<size_t>(k) * 2 + x) * 2 + 0) * BM + r];
-            if (mk_ == -INFINITY) continue;
-            const float fk = ptx::ex2(mk_ - M);
-            const float4* srcp = sp.ws_o + (static_cast<size_t>(k) * 2 + x) * (HD / 4) * BM + r;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float4 v4 = srcp[(c * 8 + e) * BM];
-              o[4 * e + 0] += v4.x * fk;
-              o[4 * e + 1] += v4.y * fk;
-              o[4 * e + 2] += v4.z * fk;
-              o[4 * e + 3] += v4.w * fk;
-            }
           }
           stage_half(h, o, inv_l);
         }
@@ -1220,6 +1183,82 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, TMEM_COLS);
   }
+}
+
+// ========================================================= split-pair merge
+//
+// After the stream-K kernel: one CTA per (split pair, query tile, 32-row
+// block, 64-column half).  Each thread owns one row and eight output columns
+// and combines the pair's pieces in slot order (the piece holding KV tile 0
+// first, then the later pieces in CTA order), as online-softmax tiles combine:
+// M = max m_k, O = sum 2^(m_k - M) O_k / sum 2^(m_k - M) l_k.  A piece that saw
+// no key of a row (m = -inf) contributes nothing and its O is not read.
+constexpr int MERGE_THREADS = 256;  // 8 warps: one 8-column chunk each, lanes = rows
+
+struct MergeParams {
+  Params p;
+  const float4* ws_o;  // as SkParams
+  const float* ws_ml;
+  int n_split;
+  int mu[SK_MAX_CTAS];    // split pair unit
+  short ms[SK_MAX_CTAS];  // its first piece's slot; pieces at ms .. ms + mn - 1 in KV order
+  short mn[SK_MAX_CTAS];
+};
+
+template <int HD, bool BF16>
+__global__ void __launch_bounds__(MERGE_THREADS)
+    fa_sk_merge_kernel(const __grid_constant__ MergeParams mp) {
+  const Params& p = mp.p;
+  constexpr int HALVES = HD / 64;  // 64-column halves (hd 128) or the whole row (hd 64)
+  const int blk = static_cast<int>(blockIdx.x);
+  const int hf = blk % HALVES;
+  const int rb = (blk / HALVES) % (BM / 32);
+  const int x = (blk / (HALVES * (BM / 32))) & 1;
+  const int i = blk / (HALVES * (BM / 32) * 2);
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();  // every piece of the stream-K kernel is written and visible
+  if (i >= mp.n_split) return;
+  const UnitGeo w = unit_geo(p, mp.mu[i]);
+  if (x == 1 && !w.has1) return;
+  const int q0 = x == 0 ? w.q00 : w.q01;
+  const int hq = x == 0 ? w.hq0 : w.hq1;
+  const int lane = threadIdx.x & 31;
+  const int r = rb * 32 + lane;
+  const int ch = hf * 8 + (threadIdx.x >> 5);  // 8-column chunk: float4 groups 2 ch, 2 ch + 1
+  const int s0 = mp.ms[i], np = mp.mn[i];
+  auto ml = [&](int k, int which) { return mp.ws_ml[((static_cast<size_t>(s0 + k) * 2 + x) * 2 + which) * BM + r]; };
+  float M = -INFINITY;
+  for (int k = 0; k < np; ++k) M = fmaxf(M, ml(k, 0));
+  float L = 0.f;
+  float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+  for (int k = 0; k < np; ++k) {
+    const float mk = ml(k, 0);
+    const bool vk = mk != -INFINITY;
+    const float f = vk ? ptx::ex2(mk - M) : 0.f;
+    const float lk = ml(k, 1);
+    const float4* src = mp.ws_o + (static_cast<size_t>(s0 + k) * 2 + x) * (HD / 4) * BM + r;
+    float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
+    if (vk) {
+      v0 = src[(2 * ch) * BM];
+      v1 = src[(2 * ch + 1) * BM];
+    }
+    L = vk ? fmaf(lk, f, L) : L;
+    a[0] = vk ? fmaf(v0.x, f, a[0]) : a[0];
+    a[1] = vk ? fmaf(v0.y, f, a[1]) : a[1];
+    a[2] = vk ? fmaf(v0.z, f, a[2]) : a[2];
+    a[3] = vk ? fmaf(v0.w, f, a[3]) : a[3];
+    a[4] = vk ? fmaf(v1.x, f, a[4]) : a[4];
+    a[5] = vk ? fmaf(v1.y, f, a[5]) : a[5];
+    a[6] = vk ? fmaf(v1.z, f, a[6]) : a[6];
+    a[7] = vk ? fmaf(v1.w, f, a[7]) : a[7];
+  }
+  if (q0 + r >= p.Sq) return;
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  uint16_t* orow = p.o + ((static_cast<size_t>(w.b) * p.Sq + q0 + r) * p.Hq + hq) * HD + 8 * ch;
+  *reinterpret_cast<uint4*>(orow) = make_uint4(pack2<BF16>(a[0] * inv, a[1] * inv), pack2<BF16>(a[2] * inv, a[3] * inv),
+                                               pack2<BF16>(a[4] * inv, a[5] * inv), pack2<BF16>(a[6] * inv, a[7] * inv));
+  if (ch == 0 && p.lse) p.lse[(static_cast<size_t>(w.b) * p.Hq + hq) * p.Sq + q0 + r] = row_lse(M, L);
 }
 
 // =============================================================== host side
@@ -1528,6 +1567,14 @@ struct SkSchedule {
   int G;
   int su[SK_MAX_CTAS + 1];
   int sj[SK_MAX_CTAS + 1];
+  // piece slots (SkParams::pf, ph) and the split pairs the merge kernel combines
+  short pf[SK_MAX_CTAS];
+  short ph[SK_MAX_CTAS];
+  int slots;    // piece slots in use
+  int n_split;  // split pairs
+  int mu[SK_MAX_CTAS];
+  short ms[SK_MAX_CTAS];
+  short mn[SK_MAX_CTAS];
 };
 
 static std::mutex g_sched_mu;
@@ -1582,6 +1629,30 @@ static void make_schedule(const Params& prm, int sms, SkSchedule* sc) {
   sc->G = G;
   sc->su[G] = static_cast<int>(nu);
   sc->sj[G] = 0;
+  // Piece slots, in CTA order: a CTA that starts inside a pair continues the
+  // pair opened last (its first segment gets the next slot); a CTA whose range
+  // ends inside a pair it entered at KV tile 0 opens that pair (its last
+  // segment gets the next slot).  So every split pair's pieces hold
+  // consecutive slots in KV order, the piece with KV tile 0 first.
+  int slot = 0, ns = 0;
+  for (int c = 0; c < G; ++c) {
+    sc->pf[c] = sc->ph[c] = -1;
+    if (sc->sj[c] > 0 && ns > 0 && sc->mu[ns - 1] == sc->su[c]) {
+      sc->pf[c] = static_cast<short>(slot++);
+      ++sc->mn[ns - 1];
+    }
+    const bool ends_inside = sc->sj[c + 1] > 0;
+    const bool single_tail = sc->su[c + 1] == sc->su[c] && sc->sj[c] > 0;  // one segment, not at tile 0
+    if (ends_inside && !single_tail) {
+      sc->ph[c] = static_cast<short>(slot++);
+      sc->mu[ns] = sc->su[c + 1];
+      sc->ms[ns] = sc->ph[c];
+      sc->mn[ns] = 1;
+      ++ns;
+    }
+  }
+  sc->slots = slot;
+  sc->n_split = ns;
 }
 
 static void get_schedule(const Params& prm, int sms, SkSchedule* out) {
@@ -1600,7 +1671,28 @@ static void get_schedule(const Params& prm, int sms, SkSchedule* out) {
   if (g_sched_n < 8) ++g_sched_n;
 }
 
-static std::atomic<unsigned> g_seq{0};
+// The split pairs' merge, after the stream-K kernel on the same stream
+// (programmatic dependent launch: it waits for every piece).
+template <int HD, bool BF16>
+static int launch_merge(const SkSchedule& sc, const Params& prm, const float4* ws_o, const float* ws_ml,
+                        cudaStream_t stream) {
+  if (sc.n_split == 0) return FA_OK;
+  MergeParams mp;
+  std::memset(&mp, 0, sizeof(mp));
+  mp.p = prm;
+  mp.ws_o = ws_o;
+  mp.ws_ml = ws_ml;
+  mp.n_split = sc.n_split;
+  std::memcpy(mp.mu, sc.mu, sizeof(int) * sc.n_split);
+  std::memcpy(mp.ms, sc.ms, sizeof(short) * sc.n_split);
+  std::memcpy(mp.mn, sc.mn, sizeof(short) * sc.n_split);
+  const unsigned grid = static_cast<unsigned>(sc.n_split) * 2u * (BM / 32) * (HD / 64);
+  if (launch_pdl(fa_sk_merge_kernel<HD, BF16>, dim3(grid), dim3(MERGE_THREADS), 0, stream, mp) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return FA_ERR_LAUNCH;
+  }
+  return FA_OK;
+}
 
 template <int HD, bool BF16>
 static int launch_sk(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int Sq, int Skv,
@@ -1648,29 +1740,17 @@ static int launch_sk(const void* q, const void* k, const void* v, void* o, int B
   get_schedule(prm, g_dev_sms[dev].load(), &sc);
   std::memcpy(sp.su, sc.su, sizeof(int) * (sc.G + 1));
   std::memcpy(sp.sj, sc.sj, sizeof(int) * (sc.G + 1));
+  std::memcpy(sp.pf, sc.pf, sizeof(short) * sc.G);
+  std::memcpy(sp.ph, sc.ph, sizeof(short) * sc.G);
   uint8_t* base = static_cast<uint8_t*>(ws);
   sp.ws_o = reinterpret_cast<float4*>(base);
   sp.ws_ml = reinterpret_cast<float*>(base + SL::WS_O_BYTES);
-  sp.ws_flag = reinterpret_cast<unsigned*>(base + SL::WS_O_BYTES + SL::WS_ML_BYTES);
-  unsigned seq = ++g_seq;
-  if (seq == 0) seq = ++g_seq;
-  sp.seq = seq;
-  cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3(static_cast<unsigned>(sc.G));
-  cfg.blockDim = dim3(NUM_THREADS);
-  cfg.dynamicSmemBytes = SL::REQUEST;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident: merges wait on other CTAs
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, mkt, mvt, sp) != cudaSuccess) {
+  if (launch_pdl(kern, dim3(static_cast<unsigned>(sc.G)), dim3(NUM_THREADS), SL::REQUEST, stream, mq, mk, mv, mo, mkt,
+                 mvt, sp) != cudaSuccess) {
     (void)cudaGetLastError();
     return FA_ERR_LAUNCH;
   }
-  return FA_OK;
+  return launch_merge<HD, BF16>(sc, prm, sp.ws_o, sp.ws_ml, stream);
 }
 
 // Attention over a K/V cache of kv_cap rows per sequence of which the first
@@ -1835,38 +1915,32 @@ namespace fa {
 // allocator), and a C host with no device allocator of its own that holds
 // only the tensors it is given.  Nothing here allocates or frees device
 // memory.  Layout of the array (the kernel indexes every region by CTA slot):
-//   [0, 8 KB)         flags: 256 CTAs x 2 tiles x 4 warps (must start at zero)
-//   [8 KB, 520 KB)    m and l: 256 x 2 x 2 x 128 f32
-//   [520 KB, ...)     partial O: (the call's CTAs) x 2 x 128 x hd f32
+//   [0, 1 MB)         m and l: 512 piece slots x 2 tiles x 2 x 128 f32
+//   [1 MB, ...)       partial O: (the call's piece slots) x 2 x 128 x hd f32
 static __device__ __align__(256) unsigned char g_static_scratch[FA_STATIC_SCRATCH_BYTES];
 
-constexpr size_t STATIC_FLAG_BYTES = (size_t)SK_MAX_CTAS * 2 * 4 * 4;
-constexpr size_t STATIC_ML_BYTES = (size_t)SK_MAX_CTAS * 2 * 2 * BM * 4;
-constexpr size_t STATIC_O_OFF = STATIC_FLAG_BYTES + STATIC_ML_BYTES;
-static_assert(STATIC_FLAG_BYTES % 256 == 0 && STATIC_O_OFF % 256 == 0, "region alignment");
-static_assert(STATIC_O_OFF + (size_t)2 * BM * 128 * 4 <= FA_STATIC_SCRATCH_BYTES, "one CTA must fit");
+constexpr size_t STATIC_ML_BYTES = (size_t)SK_SLOTS * 2 * 2 * BM * 4;
+constexpr size_t STATIC_O_OFF = STATIC_ML_BYTES;
+static_assert(STATIC_O_OFF % 256 == 0, "region alignment");
+static_assert(STATIC_O_OFF + (size_t)2 * SK_MAX_CTAS * 2 * BM * 64 * 4 <= FA_STATIC_SCRATCH_BYTES,
+              "two pieces per CTA of a full grid must fit at hd 64");
 
-static size_t static_bytes_needed(int hd, int ctas) { return STATIC_O_OFF + (size_t)ctas * 2 * BM * hd * 4; }
+static size_t static_bytes_needed(int hd, int slots) { return STATIC_O_OFF + (size_t)slots * 2 * BM * hd * 4; }
 
 static std::mutex g_static_mu;
 static uint8_t* g_static_base[MAX_DEVICES];
 
-// Set-up, once per device (the first call): the array's device address, and
-// its flag words zeroed -- a flag equal to a call's sequence number means
-// "this piece is written", so no stale word may hold one.  The clear runs on
-// the caller's stream and is waited for.  Later calls read the cached address.
+// The array's device address, looked up once per device (the first call);
+// no part of it needs initialising (every slot a call reads, that call's
+// stream-K kernel has written).
 static int static_scratch(int dev, cudaStream_t stream, uint8_t** base) {
+  (void)stream;
   std::lock_guard<std::mutex> lk(g_static_mu);
   if (g_static_base[dev] == nullptr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) {
       (void)cudaGetLastError();
       return FA_ERR_DEVICE;
-    }
-    if (cudaMemsetAsync(p, 0, STATIC_FLAG_BYTES, stream) != cudaSuccess ||
-        cudaStreamSynchronize(stream) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return FA_ERR_LAUNCH;
     }
     g_static_base[dev] = static_cast<uint8_t*>(p);
   }
@@ -1897,15 +1971,13 @@ static int launch_sk_static(const void* q, const void* k, const void* v, void* o
   prm.watchdog_ns = WATCHDOG_NS;
   SkSchedule sc;
   get_schedule(prm, g_dev_sms[dev].load(), &sc);
-  if (static_bytes_needed(HD, sc.G) > FA_STATIC_SCRATCH_BYTES) return FA_ERR_SCRATCH;
+  if (static_bytes_needed(HD, sc.slots) > FA_STATIC_SCRATCH_BYTES) return FA_ERR_SCRATCH;
   std::memcpy(sp.su, sc.su, sizeof(int) * (sc.G + 1));
   std::memcpy(sp.sj, sc.sj, sizeof(int) * (sc.G + 1));
-  sp.ws_flag = reinterpret_cast<unsigned*>(base);
-  sp.ws_ml = reinterpret_cast<float*>(base + STATIC_FLAG_BYTES);
+  std::memcpy(sp.pf, sc.pf, sizeof(short) * sc.G);
+  std::memcpy(sp.ph, sc.ph, sizeof(short) * sc.G);
+  sp.ws_ml = reinterpret_cast<float*>(base);
   sp.ws_o = reinterpret_cast<float4*>(base + STATIC_O_OFF);
-  unsigned seq = ++g_seq;
-  if (seq == 0) seq = ++g_seq;
-  sp.seq = seq;
   const int slot = (HD == 128 ? 2 : 0) + (BF16 ? 1 : 0);
   if (g_sk_attr_set[dev][slot].load() == 0) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SL::REQUEST) != cudaSuccess) {
@@ -1920,22 +1992,12 @@ static int launch_sk_static(const void* q, const void* k, const void* v, void* o
   if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, HD, Sq) || !encode_bshd(&mk, enc, k, BF16, B, Skv, Hkv, HD, kv_cap) ||
       !encode_bshd(&mv, enc, v, BF16, B, Skv, Hkv, HD, kv_cap) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, HD, Sq))
     return FA_ERR_LAUNCH;
-  cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3(static_cast<unsigned>(sc.G));
-  cfg.blockDim = dim3(NUM_THREADS);
-  cfg.dynamicSmemBytes = SL::REQUEST;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, mk, mv, sp) != cudaSuccess) {
+  if (launch_pdl(kern, dim3(static_cast<unsigned>(sc.G)), dim3(NUM_THREADS), SL::REQUEST, stream, mq, mk, mv, mo, mk,
+                 mv, sp) != cudaSuccess) {
     (void)cudaGetLastError();
     return FA_ERR_LAUNCH;
   }
-  return FA_OK;
+  return launch_merge<HD, BF16>(sc, prm, sp.ws_o, sp.ws_ml, stream);
 }
 
 static int run_static(bool bf16, const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,

@@ -124,7 +124,9 @@ int fa_prefill_bf16(const void* q, const void* k, const void* v, void* o,
  * each taking an equal share of all (query-tile pair, KV tile) steps, so short
  * prompts, single heads and causal rows of very different lengths keep every
  * SM busy.  A query-tile pair whose KV steps are split between CTAs is merged
- * in a fixed order (results are deterministic, run to run); this is the
+ * by a second, short kernel enqueued behind the first (programmatic dependent
+ * launch), over the whole GPU and in a fixed order (results are
+ * deterministic, run to run); this is the
  * split-K with a fixed-order reduction and no atomic accumulation that the
  * pages' GEMM work uses for underfilled grids, applied to the KV dimension.
  * The merge keeps each piece's unnormalised O with its running max m and sum
@@ -134,14 +136,12 @@ int fa_prefill_bf16(const void* q, const void* k, const void* v, void* o,
  *
  * The first 13 arguments are those of fa_prefill / fa_prefill_bf16, then:
  *   workspace        caller-owned DEVICE memory, >= fa_workspace_bytes(hd)
- *                    bytes, 256-byte aligned, ZERO-FILLED before its first use
- *                    (the library keeps it consistent afterwards: each call
- *                    tags what it writes with a fresh sequence number)
+ *                    bytes, 256-byte aligned; no initialisation needed (a
+ *                    call reads only what it wrote itself)
  *   workspace_bytes  its size in bytes
  * Calls that share one workspace must not overlap on the GPU (issue them on
- * one stream, or give each stream its own workspace).  The kernel is launched
- * cooperatively (all its CTAs resident at once); if the device cannot hold
- * the grid the call returns FA_ERR_LAUNCH.
+ * one stream, or give each stream its own workspace).  No CTA waits on
+ * another: the pieces meet only in the merge kernel.
  * Additional errors: FA_ERR_INVALID_ARG for a NULL or too small workspace,
  * FA_ERR_ALIGNMENT for a workspace not 256-byte aligned.
  */
@@ -156,7 +156,10 @@ int fa_prefill_ws_bf16(const void* q, const void* k, const void* v, void* o,
                        size_t workspace_bytes, void* stream);
 
 /* Workspace bytes fa_prefill_ws needs for head dimension hd (0 if
- * unsupported); independent of the other sizes.  Host-only. */
+ * unsupported); independent of the other sizes: 512 piece slots (a CTA of at
+ * most 256 holds at most two pieces of split pairs), each with both query
+ * tiles' partial O (f32, 128 rows x hd) and m and l per row, i.e.
+ * 512 * (1024 * hd + 2048) bytes.  Host-only. */
 size_t fa_workspace_bytes(int hd);
 
 /*
@@ -252,8 +255,8 @@ int fa_prefill_paged(const void* q, const void* k_pool, const void* v_pool,
  * fa_prefill_paged_ws -- fa_prefill_paged computed by the split-KV kernel
  * (fa_prefill_ws's kernel, with the same paged producer): the arguments of
  * fa_prefill_paged, then a workspace under fa_prefill_ws's rules (caller-owned,
- * >= fa_workspace_bytes(hd), 256-byte aligned, zero-filled before first use,
- * not shared by overlapping calls).  For a chunk over a long paged context,
+ * >= fa_workspace_bytes(hd), 256-byte aligned, not shared by overlapping
+ * calls).  For a chunk over a long paged context,
  * where the one-shot grid leaves most SMs idle (fa_split_kv_advised).
  * Errors: those of fa_prefill_paged and fa_prefill_ws (NULL, small or
  * misaligned workspace); hd 64 and 128 only.
@@ -294,8 +297,8 @@ int fa_kv_append(const void* k_new, const void* v_new, const void* positions,
                  int kv_cap, int bf16, void* stream);
 
 /* Size of the library's static device scratch array (one per device the
- * library runs on): 20 MiB, under 0.01 % of a 288 GB GB300. */
-#define FA_STATIC_SCRATCH_BYTES (20u * 1024u * 1024u)
+ * library runs on): 40 MiB, about 0.015 % of a 288 GB GB300. */
+#define FA_STATIC_SCRATCH_BYTES (40u * 1024u * 1024u)
 
 /*
  * fa_prefill_ws_static -- fa_prefill_ws with no caller workspace and no
@@ -307,22 +310,22 @@ int fa_kv_append(const void* k_new, const void* v_new, const void* positions,
  *     the allocator, and would break the fixed layout;
  *   - a C host with no device allocator of its own, holding only the tensors
  *     it is given.
- * Same split-KV kernel and schedule as fa_prefill_ws; the scratch (flags,
- * m and l, partial O) is a file-scope device array of FA_STATIC_SCRATCH_BYTES
+ * Same split-KV kernels and schedule as fa_prefill_ws; the scratch (m and
+ * l, partial O) is a file-scope device array of FA_STATIC_SCRATCH_BYTES
  * inside the library.  Neither the call nor the library allocates or frees
  * device memory.
  *
  * Arguments: the first 12 of fa_prefill, then
  *   bf16    0: f16 Q/K/V/O (as fa_prefill); non-zero: bfloat16 (as fa_prefill_bf16)
  *   stream  cudaStream_t to enqueue on (NULL = legacy default stream)
- * Scratch need: 532480 + ctas * 1024 * hd bytes, ctas being the CTAs of the
- * call's schedule (at most the SM count, and at most 256).  A call that needs
- * more than FA_STATIC_SCRATCH_BYTES returns FA_ERR_SCRATCH and launches
- * nothing; on a 152-SM GB300 every call fits (at most 20455424 bytes, hd 128).
+ * Scratch need: 1048576 + pieces * 1024 * hd bytes, pieces being the
+ * workspace slots of the call's schedule (at most twice its CTAs, which are
+ * at most the SM count and at most 256).  A call that needs more than
+ * FA_STATIC_SCRATCH_BYTES returns FA_ERR_SCRATCH and launches nothing; on a
+ * 152-SM GB300 every call fits (at most 40763392 bytes, hd 128).
  * Set-up: the first call on each device looks up the array's address
- * (cudaGetSymbolAddress) and zeroes its flag words, the part that must start
- * at zero, on `stream`, and waits for that; make this first call before any
- * stream capture begins.  Later calls only launch the kernel.
+ * (cudaGetSymbolAddress); nothing in it needs initialising.  Later calls only
+ * launch the kernels.
  * Concurrency: every call on a device uses the same array, so calls that
  * overlap on the GPU (issued on different streams, or from several host
  * threads, without ordering between them) race and corrupt each other's
@@ -351,7 +354,8 @@ unsigned int fa_smem_bytes(int hd);
 /*
  * fa_debug_status -- the kernel watchdog word of the current device: 0 when
  * no kernel has reported a problem since the last clear, otherwise a code
- * (bits 0-7: which wait gave up -- or 32, a cache-append position out of
+ * (bits 0-7: which wait gave up -- or 12, a split piece the schedule gave no
+ * workspace slot (not expected), 32, a cache-append position out of
  * range (fa_kv_append), or 33, a block-table entry outside the pool
  * (fa_prefill_paged); bits 8-31: the CTA or token index, saturated).  A
  * pipeline wait that does not complete within the watchdog limit records its

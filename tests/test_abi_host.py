@@ -97,13 +97,13 @@ def test_python_wrapper_rejects_cpu_tensors(fa):
 
 
 def test_workspace_size_and_errors_without_a_device(fa):
-    """Stream-K workspace: per SM slot (up to 256), both tiles' partial O in f32
-    plus m and l per row, plus one flag per (tile, warp)."""
+    """Stream-K workspace: 512 piece slots (a CTA of up to 256 holds at most two
+    pieces of split pairs), each with both tiles' partial O in f32 and m and l
+    per row."""
     for hd in (64, 128):
-        o_bytes = 256 * 2 * 128 * hd * 4
-        ml_bytes = 256 * 2 * 2 * 128 * 4
-        flag_bytes = ((256 * 2 * 4 * 4 + 255) // 256) * 256
-        assert fa.workspace_bytes(hd) == o_bytes + ml_bytes + flag_bytes
+        o_bytes = 512 * 2 * 128 * hd * 4
+        ml_bytes = 512 * 2 * 2 * 128 * 4
+        assert fa.workspace_bytes(hd) == o_bytes + ml_bytes
     assert fa.workspace_bytes(80) == 0
     ws = fa.workspace_bytes(128)
     args = (A, 2 * A, 3 * A, 4 * A, 1, 4, 2, 8, 8, 128, 1, 0.1)
