@@ -176,7 +176,7 @@ def attention_paged(q, k_pool, v_pool, block_table, kv_len: int, causal: bool = 
     [num_blocks, page_size, Hkv, hd] through block_table [B, max_pages]
     (int32): key j of sequence b is k_pool[block_table[b, j // page_size],
     j % page_size].  page_size must be a multiple of 128.  ``split`` as in
-    ``attention`` (split-KV for hd 64 and 128).  Raises FaError."""
+    ``attention`` (split-KV for heads up to 128 wide).  Raises FaError."""
     import torch
     if q.dim() != 4 or k_pool.dim() != 4 or v_pool.shape != k_pool.shape or block_table.dim() != 2:
         raise ValueError("q [B, Sq, Hq, hd], pools [num_blocks, page_size, Hkv, hd], table [B, max_pages]")
@@ -198,7 +198,7 @@ def attention_paged(q, k_pool, v_pool, block_table, kv_len: int, causal: bool = 
     elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
         raise ValueError("out must be a contiguous CUDA tensor like q")
     if split is None:
-        split = hd != 256 and split_kv_advised(B, Hq, Hkv, Sq, kv_len, causal)
+        split = hd <= 128 and split_kv_advised(B, Hq, Hkv, Sq, kv_len, causal)
     if split:
         ws = workspace_for(q.device, hd, stream)
         st = fa_prefill_paged_ws(q, k_pool, v_pool, block_table, out, B, Hq, Hkv, Sq, kv_len, hd, page_size,
@@ -267,7 +267,7 @@ def attention_kvcache(q, k_cache, v_cache, kv_len: int, causal: bool = True, sca
     elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
         raise ValueError("out must be a contiguous CUDA tensor like q")
     if split is None:
-        split = hd != 256 and split_kv_advised(B, Hq, Hkv, Sq, kv_len, causal)
+        split = hd <= 128 and split_kv_advised(B, Hq, Hkv, Sq, kv_len, causal)
     ws = workspace_for(q.device, hd, stream) if split else None
     st = fa_prefill_kvcache(q, k_cache, v_cache, out, B, Hq, Hkv, Sq, kv_len, kv_cap, hd, int(bool(causal)),
                             scale, int(q.dtype == torch.bfloat16), ws, ws.numel() if ws is not None else 0, stream)
@@ -345,8 +345,8 @@ def attention(q, k, v, causal: bool = True, scale: float | None = None, out=None
         out = torch.empty_like(q)
     elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
         raise ValueError("out must be a contiguous CUDA tensor like q")
-    if split is None:  # split-KV exists for hd 64 and 128
-        split = hd != 256 and split_kv_advised(B, Hq, Hkv, Sq, Skv, causal)
+    if split is None:  # split-KV exists for heads up to 128 wide
+        split = hd <= 128 and split_kv_advised(B, Hq, Hkv, Sq, Skv, causal)
     if return_lse:
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
         ws = workspace_for(q.device, hd, stream) if split else None

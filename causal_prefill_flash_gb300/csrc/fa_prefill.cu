@@ -140,6 +140,7 @@ struct Params {
   const int* block_table;  // nullptr: contiguous [B][Skv][Hkv][hd] K/V
   int page_size, max_pages, num_blocks, last_page;
   float* lse;  // nullptr, or [B][Hq][Sq]: log sum_j exp(scale s_j) of every row (-inf: no key)
+  int hd;      // head dimension of the tensors (<= the kernel's HD: the maps zero-fill and clip the rest)
 };
 
 // A row's log-sum-exp from the online-softmax state: m (log2 units of
@@ -1254,11 +1255,12 @@ __global__ void __launch_bounds__(MERGE_THREADS)
     a[7] = vk ? fmaf(v1.w, f, a[7]) : a[7];
   }
   if (q0 + r >= p.Sq) return;
+  if (ch == 0 && p.lse) p.lse[(static_cast<size_t>(w.b) * p.Hq + hq) * p.Sq + q0 + r] = row_lse(M, L);
+  if (8 * ch >= p.hd) return;  // zero padding columns of a narrower head
   const float inv = L > 0.f ? 1.f / L : 0.f;
-  uint16_t* orow = p.o + ((static_cast<size_t>(w.b) * p.Sq + q0 + r) * p.Hq + hq) * HD + 8 * ch;
+  uint16_t* orow = p.o + ((static_cast<size_t>(w.b) * p.Sq + q0 + r) * p.Hq + hq) * p.hd + 8 * ch;
   *reinterpret_cast<uint4*>(orow) = make_uint4(pack2<BF16>(a[0] * inv, a[1] * inv), pack2<BF16>(a[2] * inv, a[3] * inv),
                                                pack2<BF16>(a[4] * inv, a[5] * inv), pack2<BF16>(a[6] * inv, a[7] * inv));
-  if (ch == 0 && p.lse) p.lse[(static_cast<size_t>(w.b) * p.Hq + hq) * p.Sq + q0 + r] = row_lse(M, L);
 }
 
 // =============================================================== host side
@@ -1417,7 +1419,7 @@ static bool encode_kv(CUtensorMap* mk, CUtensorMap* mv, CUtensorMap* mkt, CUtens
 }
 
 template <int HD, bool BF16>
-static int launch(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int Sq, int Skv,
+static int launch(const void* q, const void* k, const void* v, void* o, int hd, int B, int Hq, int Hkv, int Sq, int Skv,
                   int kv_cap, int causal, float scale, cudaStream_t stream, int dev, const Paged* pg = nullptr,
                   float* lse = nullptr) {
   using L = Layout<HD>;
@@ -1434,11 +1436,12 @@ static int launch(const void* q, const void* k, const void* v, void* o, int B, i
   if (!enc) return FA_ERR_LAUNCH;
   CUtensorMap mq, mk, mv, mo, mkt, mvt;
   Params prm;
-  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, HD, Sq) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, HD, Sq) ||
-      !encode_kv(&mk, &mv, &mkt, &mvt, enc, k, v, BF16, B, Skv, kv_cap, Hkv, HD, pg, &prm))
+  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, hd, Sq) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, hd, Sq) ||
+      !encode_kv(&mk, &mv, &mkt, &mvt, enc, k, v, BF16, B, Skv, kv_cap, Hkv, hd, pg, &prm))
     return FA_ERR_LAUNCH;
   prm.lse = lse;
   prm.o = static_cast<uint16_t*>(o);
+  prm.hd = hd;
   prm.B = B;
   prm.Hq = Hq;
   prm.Hkv = Hkv;
@@ -1461,7 +1464,7 @@ static int launch(const void* q, const void* k, const void* v, void* o, int B, i
 
 // hd = 256: one query tile per CTA (fa_prefill256_kernel).
 template <bool BF16>
-static int launch256(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int Sq, int Skv,
+static int launch256(const void* q, const void* k, const void* v, void* o, int hd, int B, int Hq, int Hkv, int Sq, int Skv,
                      int kv_cap, int causal, float scale, cudaStream_t stream, int dev, float* lse = nullptr) {
   using L = Layout256;
   auto kern = fa_prefill256_kernel<BF16>;
@@ -1475,12 +1478,13 @@ static int launch256(const void* q, const void* k, const void* v, void* o, int B
   EncodeTiledFn enc = encoder();
   if (!enc) return FA_ERR_LAUNCH;
   CUtensorMap mq, mk, mv, mo;
-  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, L::HD, Sq) || !encode_bshd(&mk, enc, k, BF16, B, Skv, Hkv, L::HD, kv_cap) ||
-      !encode_bshd(&mv, enc, v, BF16, B, Skv, Hkv, L::HD, kv_cap) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, L::HD, Sq))
+  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, hd, Sq) || !encode_bshd(&mk, enc, k, BF16, B, Skv, Hkv, hd, kv_cap) ||
+      !encode_bshd(&mv, enc, v, BF16, B, Skv, Hkv, hd, kv_cap) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, hd, Sq))
     return FA_ERR_LAUNCH;
   Params prm;
   std::memset(&prm, 0, sizeof(prm));
   prm.o = static_cast<uint16_t*>(o);
+  prm.hd = hd;
   prm.B = B;
   prm.Hq = Hq;
   prm.Hkv = Hkv;
@@ -1504,13 +1508,22 @@ static int launch256(const void* q, const void* k, const void* v, void* o, int B
 
 // Argument checks shared by every entry point (no device call).  May replace
 // k and v by q when Skv == 0 (no key is ever loaded; the maps need a base).
+// The kernel a head dimension runs on: a multiple of 8 (16-byte rows for TMA)
+// up to 256, on the 64, 128 or 256 kernel.  A narrower head's maps describe
+// its true width, so TMA loads the missing columns of Q, K and V as zeros and
+// clips them from the O store: S and P V are unchanged by the zero columns.
+static int kernel_hd(int hd) {
+  if (hd < 8 || hd % 8 != 0 || hd > 256) return 0;
+  return hd <= 64 ? 64 : hd <= 128 ? 128 : 256;
+}
+
 static int validate(const void* q, const void*& k, const void*& v, const void* o, int B, int Hq, int Hkv, int Sq,
                     int Skv, int hd, float scale, bool* empty) {
   *empty = false;
   if (B < 0 || Sq < 0 || Skv < 0 || Hq < 1 || Hkv < 1) return FA_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
-  if (hd != 64 && hd != 128 && hd != 256) return FA_ERR_UNSUPPORTED;
+  if (kernel_hd(hd) == 0) return FA_ERR_UNSUPPORTED;
   if (B == 0 || Sq == 0) {  // nothing to compute; no pointer is read
     *empty = true;
     return FA_OK;
@@ -1542,21 +1555,21 @@ static int run(bool bf16, const void* q, const void* k, const void* v, void* o, 
   const int ds = check_device(&dev);
   if (ds != FA_OK) return ds;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (hd == 256)
-    return bf16 ? launch256<true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev)
-                : launch256<false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev);
-  if (hd == 128)
-    return bf16 ? launch<128, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev)
-                : launch<128, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev);
-  return bf16 ? launch<64, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev)
-              : launch<64, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev);
+  if (kernel_hd(hd) == 256)
+    return bf16 ? launch256<true>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev)
+                : launch256<false>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev);
+  if (kernel_hd(hd) == 128)
+    return bf16 ? launch<128, true>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev)
+                : launch<128, false>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev);
+  return bf16 ? launch<64, true>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev)
+              : launch<64, false>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev);
 }
 
 // ------------------------------------------------------ stream-K host side
 
 static size_t ws_bytes_for(int hd) {
-  if (hd == 128) return SkLayout<128>::WS_BYTES;
-  if (hd == 64) return SkLayout<64>::WS_BYTES;
+  if (kernel_hd(hd) == 128) return SkLayout<128>::WS_BYTES;
+  if (kernel_hd(hd) == 64) return SkLayout<64>::WS_BYTES;
   return 0;
 }
 
@@ -1695,7 +1708,7 @@ static int launch_merge(const SkSchedule& sc, const Params& prm, const float4* w
 }
 
 template <int HD, bool BF16>
-static int launch_sk(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int Sq, int Skv,
+static int launch_sk(const void* q, const void* k, const void* v, void* o, int hd, int B, int Hq, int Hkv, int Sq, int Skv,
                      int kv_cap, int causal, float scale, void* ws, cudaStream_t stream, int dev,
                      const Paged* pg = nullptr, float* lse = nullptr) {
   using SL = SkLayout<HD>;
@@ -1712,13 +1725,14 @@ static int launch_sk(const void* q, const void* k, const void* v, void* o, int B
   if (!enc) return FA_ERR_LAUNCH;
   CUtensorMap mq, mk, mv, mo, mkt, mvt;
   Params pkv;
-  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, HD, Sq) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, HD, Sq) ||
-      !encode_kv(&mk, &mv, &mkt, &mvt, enc, k, v, BF16, B, Skv, kv_cap, Hkv, HD, pg, &pkv))
+  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, hd, Sq) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, hd, Sq) ||
+      !encode_kv(&mk, &mv, &mkt, &mvt, enc, k, v, BF16, B, Skv, kv_cap, Hkv, hd, pg, &pkv))
     return FA_ERR_LAUNCH;
   SkParams sp;
   std::memset(&sp, 0, sizeof(sp));
   Params& prm = sp.p;
   prm.o = static_cast<uint16_t*>(o);
+  prm.hd = hd;
   prm.B = B;
   prm.Hq = Hq;
   prm.Hkv = Hkv;
@@ -1769,7 +1783,7 @@ static int run_kvcache(bool bf16, const void* q, const void* k, const void* v, v
   const unsigned long long cn = (unsigned long long)B * kv_cap * Hkv * hd;
   if (kv_len > 0 && (overlaps(o, qn * 2, k, cn * 2) || overlaps(o, qn * 2, v, cn * 2))) return FA_ERR_INVALID_ARG;
   if (ws) {
-    if (hd == 256) return FA_ERR_UNSUPPORTED;  // split-KV: hd 64 and 128
+    if (kernel_hd(hd) == 256) return FA_ERR_UNSUPPORTED;  // split-KV: heads up to 128 wide
     if (reinterpret_cast<uintptr_t>(ws) & 255u) return FA_ERR_ALIGNMENT;
     if (ws_bytes < ws_bytes_for(hd)) return FA_ERR_INVALID_ARG;
   }
@@ -1778,21 +1792,21 @@ static int run_kvcache(bool bf16, const void* q, const void* k, const void* v, v
   if (ds != FA_OK) return ds;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int stride = kv_len > 0 ? kv_cap : 0;  // kv_len == 0: the maps point at q (no key is loaded)
-  if (hd == 256)
-    return bf16 ? launch256<true>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, st, dev)
-                : launch256<false>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, st, dev);
+  if (kernel_hd(hd) == 256)
+    return bf16 ? launch256<true>(q, k, v, o, hd, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, st, dev)
+                : launch256<false>(q, k, v, o, hd, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, st, dev);
   if (ws) {
-    if (hd == 128)
-      return bf16 ? launch_sk<128, true>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, ws, st, dev)
-                  : launch_sk<128, false>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, ws, st, dev);
-    return bf16 ? launch_sk<64, true>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, ws, st, dev)
-                : launch_sk<64, false>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, ws, st, dev);
+    if (kernel_hd(hd) == 128)
+      return bf16 ? launch_sk<128, true>(q, k, v, o, hd, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, ws, st, dev)
+                  : launch_sk<128, false>(q, k, v, o, hd, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, ws, st, dev);
+    return bf16 ? launch_sk<64, true>(q, k, v, o, hd, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, ws, st, dev)
+                : launch_sk<64, false>(q, k, v, o, hd, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, ws, st, dev);
   }
-  if (hd == 128)
-    return bf16 ? launch<128, true>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, st, dev)
-                : launch<128, false>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, st, dev);
-  return bf16 ? launch<64, true>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, st, dev)
-              : launch<64, false>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, st, dev);
+  if (kernel_hd(hd) == 128)
+    return bf16 ? launch<128, true>(q, k, v, o, hd, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, st, dev)
+                : launch<128, false>(q, k, v, o, hd, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, st, dev);
+  return bf16 ? launch<64, true>(q, k, v, o, hd, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, st, dev)
+              : launch<64, false>(q, k, v, o, hd, B, Hq, Hkv, Sq, kv_len, stride, causal, scale, st, dev);
 }
 
 // Attention over a paged K/V pool (one-shot kernel).
@@ -1807,7 +1821,7 @@ static int run_paged(bool bf16, const void* q, const void* k_pool, const void* v
   const void* v = v_pool;
   const int vs = validate(q, k, v, o, B, Hq, Hkv, Sq, kv_len, hd, scale, &empty);
   if (vs != FA_OK || empty) return vs;
-  if (hd == 256) return FA_ERR_UNSUPPORTED;  // hd 256: the one-shot kernel only
+  if (kernel_hd(hd) == 256) return FA_ERR_UNSUPPORTED;  // heads over 128 wide: the one-shot kernel only
   if (kv_len > 0) {
     if (!block_table) return FA_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(block_table) & 3u) return FA_ERR_ALIGNMENT;
@@ -1826,17 +1840,17 @@ static int run_paged(bool bf16, const void* q, const void* k_pool, const void* v
   if (ws) {  // split-KV over the pool
     if (reinterpret_cast<uintptr_t>(ws) & 255u) return FA_ERR_ALIGNMENT;
     if (ws_bytes < ws_bytes_for(hd)) return FA_ERR_INVALID_ARG;
-    if (hd == 128)
-      return bf16 ? launch_sk<128, true>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, ws, st, dev, &pg)
-                  : launch_sk<128, false>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, ws, st, dev, &pg);
-    return bf16 ? launch_sk<64, true>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, ws, st, dev, &pg)
-                : launch_sk<64, false>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, ws, st, dev, &pg);
+    if (kernel_hd(hd) == 128)
+      return bf16 ? launch_sk<128, true>(q, k, v, o, hd, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, ws, st, dev, &pg)
+                  : launch_sk<128, false>(q, k, v, o, hd, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, ws, st, dev, &pg);
+    return bf16 ? launch_sk<64, true>(q, k, v, o, hd, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, ws, st, dev, &pg)
+                : launch_sk<64, false>(q, k, v, o, hd, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, ws, st, dev, &pg);
   }
-  if (hd == 128)
-    return bf16 ? launch<128, true>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, st, dev, &pg)
-                : launch<128, false>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, st, dev, &pg);
-  return bf16 ? launch<64, true>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, st, dev, &pg)
-              : launch<64, false>(q, k, v, o, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, st, dev, &pg);
+  if (kernel_hd(hd) == 128)
+    return bf16 ? launch<128, true>(q, k, v, o, hd, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, st, dev, &pg)
+                : launch<128, false>(q, k, v, o, hd, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, st, dev, &pg);
+  return bf16 ? launch<64, true>(q, k, v, o, hd, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, st, dev, &pg)
+              : launch<64, false>(q, k, v, o, hd, B, Hq, Hkv, Sq, kv_len, kv_len, causal, scale, st, dev, &pg);
 }
 
 // Any supported hd, either kernel (a workspace selects split-KV), and an
@@ -1853,7 +1867,7 @@ static int run_ex(bool bf16, const void* q, const void* k, const void* v, void* 
       return FA_ERR_INVALID_ARG;
   }
   if (ws) {
-    if (hd == 256) return FA_ERR_UNSUPPORTED;
+    if (kernel_hd(hd) == 256) return FA_ERR_UNSUPPORTED;
     if (reinterpret_cast<uintptr_t>(ws) & 255u) return FA_ERR_ALIGNMENT;
     if (ws_bytes < ws_bytes_for(hd)) return FA_ERR_INVALID_ARG;
     if (lse && overlaps(lse, (size_t)B * Hq * Sq * 4, ws, ws_bytes)) return FA_ERR_INVALID_ARG;
@@ -1862,21 +1876,21 @@ static int run_ex(bool bf16, const void* q, const void* k, const void* v, void* 
   const int ds = check_device(&dev);
   if (ds != FA_OK) return ds;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (hd == 256)
-    return bf16 ? launch256<true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev, lse)
-                : launch256<false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev, lse);
+  if (kernel_hd(hd) == 256)
+    return bf16 ? launch256<true>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev, lse)
+                : launch256<false>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev, lse);
   if (ws) {
-    if (hd == 128)
-      return bf16 ? launch_sk<128, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, ws, st, dev, nullptr, lse)
-                  : launch_sk<128, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, ws, st, dev, nullptr, lse);
-    return bf16 ? launch_sk<64, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, ws, st, dev, nullptr, lse)
-                : launch_sk<64, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, ws, st, dev, nullptr, lse);
+    if (kernel_hd(hd) == 128)
+      return bf16 ? launch_sk<128, true>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, ws, st, dev, nullptr, lse)
+                  : launch_sk<128, false>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, ws, st, dev, nullptr, lse);
+    return bf16 ? launch_sk<64, true>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, ws, st, dev, nullptr, lse)
+                : launch_sk<64, false>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, ws, st, dev, nullptr, lse);
   }
-  if (hd == 128)
-    return bf16 ? launch<128, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev, nullptr, lse)
-                : launch<128, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev, nullptr, lse);
-  return bf16 ? launch<64, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev, nullptr, lse)
-              : launch<64, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev, nullptr, lse);
+  if (kernel_hd(hd) == 128)
+    return bf16 ? launch<128, true>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev, nullptr, lse)
+                : launch<128, false>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev, nullptr, lse);
+  return bf16 ? launch<64, true>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev, nullptr, lse)
+              : launch<64, false>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev, nullptr, lse);
 }
 
 static int run_ws(bool bf16, const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int Sq,
@@ -1884,7 +1898,7 @@ static int run_ws(bool bf16, const void* q, const void* k, const void* v, void* 
   bool empty = false;
   const int vs = validate(q, k, v, o, B, Hq, Hkv, Sq, Skv, hd, scale, &empty);
   if (vs != FA_OK || empty) return vs;
-  if (hd == 256) return FA_ERR_UNSUPPORTED;  // hd 256: the one-shot kernel only
+  if (kernel_hd(hd) == 256) return FA_ERR_UNSUPPORTED;  // heads over 128 wide: the one-shot kernel only
   if (!ws) return FA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(ws) & 255u) return FA_ERR_ALIGNMENT;
   if (ws_bytes < ws_bytes_for(hd)) return FA_ERR_INVALID_ARG;
@@ -1892,11 +1906,11 @@ static int run_ws(bool bf16, const void* q, const void* k, const void* v, void* 
   const int ds = check_device(&dev);
   if (ds != FA_OK) return ds;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (hd == 128)
-    return bf16 ? launch_sk<128, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, ws, st, dev)
-                : launch_sk<128, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, ws, st, dev);
-  return bf16 ? launch_sk<64, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, ws, st, dev)
-              : launch_sk<64, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, ws, st, dev);
+  if (kernel_hd(hd) == 128)
+    return bf16 ? launch_sk<128, true>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, ws, st, dev)
+                : launch_sk<128, false>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, ws, st, dev);
+  return bf16 ? launch_sk<64, true>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, ws, st, dev)
+              : launch_sk<64, false>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, ws, st, dev);
 }
 
 }  // namespace fa
@@ -1949,7 +1963,7 @@ static int static_scratch(int dev, cudaStream_t stream, uint8_t** base) {
 }
 
 template <int HD, bool BF16>
-static int launch_sk_static(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int Sq,
+static int launch_sk_static(const void* q, const void* k, const void* v, void* o, int hd, int B, int Hq, int Hkv, int Sq,
                             int Skv, int causal, float scale, uint8_t* base, cudaStream_t stream, int dev) {
   const int kv_cap = Skv;
   using SL = SkLayout<HD>;
@@ -1958,6 +1972,7 @@ static int launch_sk_static(const void* q, const void* k, const void* v, void* o
   std::memset(&sp, 0, sizeof(sp));
   Params& prm = sp.p;
   prm.o = static_cast<uint16_t*>(o);
+  prm.hd = hd;
   prm.B = B;
   prm.Hq = Hq;
   prm.Hkv = Hkv;
@@ -1989,8 +2004,8 @@ static int launch_sk_static(const void* q, const void* k, const void* v, void* o
   EncodeTiledFn enc = encoder();
   if (!enc) return FA_ERR_LAUNCH;
   CUtensorMap mq, mk, mv, mo;
-  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, HD, Sq) || !encode_bshd(&mk, enc, k, BF16, B, Skv, Hkv, HD, kv_cap) ||
-      !encode_bshd(&mv, enc, v, BF16, B, Skv, Hkv, HD, kv_cap) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, HD, Sq))
+  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, hd, Sq) || !encode_bshd(&mk, enc, k, BF16, B, Skv, Hkv, HD, kv_cap) ||
+      !encode_bshd(&mv, enc, v, BF16, B, Skv, Hkv, HD, kv_cap) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, hd, Sq))
     return FA_ERR_LAUNCH;
   if (launch_pdl(kern, dim3(static_cast<unsigned>(sc.G)), dim3(NUM_THREADS), SL::REQUEST, stream, mq, mk, mv, mo, mk,
                  mv, sp) != cudaSuccess) {
@@ -2005,7 +2020,7 @@ static int run_static(bool bf16, const void* q, const void* k, const void* v, vo
   bool empty = false;
   const int vs = validate(q, k, v, o, B, Hq, Hkv, Sq, Skv, hd, scale, &empty);
   if (vs != FA_OK || empty) return vs;
-  if (hd == 256) return FA_ERR_UNSUPPORTED;  // hd 256: the one-shot kernel only
+  if (kernel_hd(hd) == 256) return FA_ERR_UNSUPPORTED;  // heads over 128 wide: the one-shot kernel only
   int dev = -1;
   const int ds = check_device(&dev);
   if (ds != FA_OK) return ds;
@@ -2013,11 +2028,11 @@ static int run_static(bool bf16, const void* q, const void* k, const void* v, vo
   uint8_t* base = nullptr;
   const int ss = static_scratch(dev, st, &base);
   if (ss != FA_OK) return ss;
-  if (hd == 128)
-    return bf16 ? launch_sk_static<128, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, causal, scale, base, st, dev)
-                : launch_sk_static<128, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, causal, scale, base, st, dev);
-  return bf16 ? launch_sk_static<64, true>(q, k, v, o, B, Hq, Hkv, Sq, Skv, causal, scale, base, st, dev)
-              : launch_sk_static<64, false>(q, k, v, o, B, Hq, Hkv, Sq, Skv, causal, scale, base, st, dev);
+  if (kernel_hd(hd) == 128)
+    return bf16 ? launch_sk_static<128, true>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, causal, scale, base, st, dev)
+                : launch_sk_static<128, false>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, causal, scale, base, st, dev);
+  return bf16 ? launch_sk_static<64, true>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, causal, scale, base, st, dev)
+              : launch_sk_static<64, false>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, causal, scale, base, st, dev);
 }
 
 }  // namespace fa
@@ -2105,7 +2120,7 @@ extern "C" const char* fa_status_string(int status) {
   switch (status) {
     case FA_OK: return "FA_OK";
     case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: null pointer, bad size, Hq % Hkv != 0, bad scale or aliasing";
-    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: hd must be 64 or 128 and tensors must fit TMA coordinates";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: hd must be a multiple of 8 up to 256 (split-KV and paged: up to 128) and tensors must fit TMA coordinates";
     case FA_ERR_ALIGNMENT: return "FA_ERR_ALIGNMENT: q, k, v and o must be 16-byte aligned";
     case FA_ERR_SMEM: return "FA_ERR_SMEM: shared-memory request does not fit the device";
     case FA_ERR_LAUNCH: return "FA_ERR_LAUNCH: TMA descriptor encode or kernel launch failed";
@@ -2116,9 +2131,9 @@ extern "C" const char* fa_status_string(int status) {
 }
 
 extern "C" unsigned int fa_smem_bytes(int hd) {
-  if (hd == 256) return fa::Layout256::REQUEST;
-  if (hd == 128) return fa::Layout<128>::REQUEST;
-  if (hd == 64) return fa::Layout<64>::REQUEST;
+  if (fa::kernel_hd(hd) == 256) return fa::Layout256::REQUEST;
+  if (fa::kernel_hd(hd) == 128) return fa::Layout<128>::REQUEST;
+  if (fa::kernel_hd(hd) == 64) return fa::Layout<64>::REQUEST;
   return 0u;
 }
 

@@ -371,7 +371,8 @@ __global__ void __launch_bounds__(NUM_THREADS_256, 1)
         ok = warp_wait_bar(bOstaged, 0, abort_flag, p.watchdog_ns, WD_SOFTMAX_O_DONE);
         if (ok && lane == 0) {
 #pragma unroll
-          for (int c = 0; c < (int)L::KCH; ++c) ptx::tma_store_4d(&tmO, sRing + c * (BM * 128), c * 64, hq, q0, b);
+          for (int c = 0; c < (int)L::KCH; ++c)  // a narrower head has no columns past p.hd: no store there
+            if (c * 64 < p.hd) ptx::tma_store_4d(&tmO, sRing + c * (BM * 128), c * 64, hq, q0, b);
           ptx::bulk_commit();
           ptx::bulk_wait_read0();
         }

@@ -34,9 +34,14 @@
  * scale multiplies Q K^T before the mask and the softmax; it must be finite and
  * > 0 (1/sqrt(hd) is the usual value).
  *
- * Supported: hd in {64, 128, 256} (hd 256 on the one-shot kernel: fa_prefill,
- * fa_prefill_bf16, fa_prefill_kvcache without a workspace; the split-KV, paged
- * and static-scratch entry points take 64 and 128); any B, Sq, Skv >= 0 and
+ * Supported: hd any multiple of 8 from 8 to 256 (16-byte rows for TMA).  A
+ * head runs on the kernel of the next width up, 64, 128 or 256 columns: its
+ * tensor maps describe the true width, so TMA loads the missing columns of Q,
+ * K and V as zeros and clips them from O, which leaves S and P V unchanged
+ * (the tensor work is that of the wider kernel).  Heads over 128 wide run on
+ * the one-shot kernel only (fa_prefill, fa_prefill_bf16, fa_prefill_ex and
+ * fa_prefill_kvcache without a workspace); the split-KV, paged and
+ * static-scratch entry points take heads up to 128 wide.  Any B, Sq, Skv >= 0 and
  * Hq, Hkv >= 1 whose tensors fit TMA's 32-bit coordinates.  B == 0 or Sq == 0
  * is a no-op
  * returning FA_OK (the pointers may then be NULL: nothing is read or written);
@@ -62,7 +67,7 @@
  *
  * Entry points
  * ------------
- *   fa_prefill, fa_prefill_bf16      one-shot kernel (hd 64, 128, 256)
+ *   fa_prefill, fa_prefill_bf16      one-shot kernel (hd 8 .. 256, multiples of 8)
  *   fa_prefill_ws, fa_prefill_ws_bf16  split-KV kernel with a caller workspace
  *   fa_workspace_bytes               its workspace size
  *   fa_split_kv_advised              which of the two kernels to use for a shape
@@ -156,10 +161,11 @@ int fa_prefill_ws_bf16(const void* q, const void* k, const void* v, void* o,
                        size_t workspace_bytes, void* stream);
 
 /* Workspace bytes fa_prefill_ws needs for head dimension hd (0 if
- * unsupported); independent of the other sizes: 512 piece slots (a CTA of at
+ * unsupported, or over 128); those of the 64- or 128-column kernel the head
+ * runs on, independent of the other sizes: 512 piece slots (a CTA of at
  * most 256 holds at most two pieces of split pairs), each with both query
- * tiles' partial O (f32, 128 rows x hd) and m and l per row, i.e.
- * 512 * (1024 * hd + 2048) bytes.  Host-only. */
+ * tiles' partial O (f32, 128 rows x kernel width) and m and l per row, i.e.
+ * 512 * (1024 * width + 2048) bytes.  Host-only. */
 size_t fa_workspace_bytes(int hd);
 
 /*
@@ -173,8 +179,8 @@ size_t fa_workspace_bytes(int hd);
  *              — FA_TKV 32->16 occupancy experiment", section 2), which is
  *              what combines attention computed over separate key ranges
  *   bf16       0: f16, non-zero: bfloat16
- *   workspace  NULL: the one-shot kernel (hd 64, 128 or 256); otherwise the
- *              split-KV kernel under fa_prefill_ws's rules (hd 64 and 128)
+ *   workspace  NULL: the one-shot kernel (any supported hd); otherwise the
+ *              split-KV kernel under fa_prefill_ws's rules (hd up to 128)
  * Errors: those of fa_prefill / fa_prefill_ws, FA_ERR_ALIGNMENT for a
  * misaligned lse, FA_ERR_INVALID_ARG for lse overlapping q, k, v, o or the
  * workspace.
@@ -259,7 +265,7 @@ int fa_prefill_paged(const void* q, const void* k_pool, const void* v_pool,
  * calls).  For a chunk over a long paged context,
  * where the one-shot grid leaves most SMs idle (fa_split_kv_advised).
  * Errors: those of fa_prefill_paged and fa_prefill_ws (NULL, small or
- * misaligned workspace); hd 64 and 128 only.
+ * misaligned workspace); heads up to 128 wide.
  */
 int fa_prefill_paged_ws(const void* q, const void* k_pool, const void* v_pool,
                         const void* block_table, void* o, int B, int Hq,
@@ -280,7 +286,7 @@ int fa_prefill_paged_ws(const void* q, const void* k_pool, const void* v_pool,
  *   positions         [B][T] int32, device, read-only: each token's cache row
  *   k_cache, v_cache  [B][kv_cap][Hkv][hd] 16-bit, device, 16-byte aligned;
  *                     only the rows named by positions are written
- *   hd                any positive multiple of 8 (the attention takes 64, 128, 256)
+ *   hd                any positive multiple of 8
  * A position outside [0, kv_cap) is skipped (nothing written for that token)
  * and reported in the device status word: fa_debug_status() returns code 32
  * with the flat index b * T + t of one such token in bits 8-31.  Positions
@@ -342,7 +348,8 @@ const char* fa_status_string(int status);
 
 /*
  * fa_smem_bytes -- the dynamic shared memory one CTA of the kernel requests
- * for head dimension hd (64, 128 or 256), computed from the kernel's own tile
+ * for head dimension hd (that of the 64-, 128- or 256-column kernel the head
+ * runs on), computed from the kernel's own tile
  * layout (Q tile, K/V stage ring, P tile, barriers, alignment slack).  Returns
  * 0 for an unsupported hd.  Host-only; no device is touched.  Exposed so the
  * launcher's request can be checked against the layout, the failure class of

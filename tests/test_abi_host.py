@@ -57,7 +57,10 @@ def test_smem_request_matches_the_tile_layout(fa):
         want = 2 * q + nslot * slot + bars * 8 + 16 + 1024
         assert fa.smem_bytes(hd) == want
         assert want <= 227 * 1024
-    assert fa.smem_bytes(96) == 0
+    assert fa.smem_bytes(100) == 0 and fa.smem_bytes(264) == 0
+    # narrower heads run on the next kernel up (64, 128 or 256)
+    assert fa.smem_bytes(32) == fa.smem_bytes(64) and fa.smem_bytes(96) == fa.smem_bytes(128)
+    assert fa.smem_bytes(192) == fa.smem_bytes(256)
     # hd 256: one 64 KB query tile, a ring of five 32 KB half tiles, 18 barriers
     assert fa.smem_bytes(256) == 64 * 1024 + 5 * 32 * 1024 + 18 * 8 + 16 + 1024 <= 227 * 1024
 
@@ -76,11 +79,12 @@ def test_argument_errors_without_a_device(fa, fn):
                  a["causal"], a["scale"], 0)
 
     assert call(q=0) == 1 and call(o=0) == 1 and call(k=0) == 1 and call(v=0) == 1
-    assert call(Skv=0, k=0, v=0, hd=96) == 2  # shape errors still reported first
+    assert call(Skv=0, k=0, v=0, hd=100) == 2  # shape errors still reported first
     assert call(B=-1) == 1 and call(Sq=-3) == 1 and call(Skv=-1) == 1
     assert call(Hq=0) == 1 and call(Hkv=0) == 1 and call(Hkv=3) == 1
     assert call(scale=float("nan")) == 1 and call(scale=0.0) == 1 and call(scale=-1.0) == 1
-    assert call(hd=96) == 2 and call(hd=512) == 2 and call(hd=32) == 2
+    # hd: a multiple of 8 (16-byte rows) up to 256
+    assert call(hd=100) == 2 and call(hd=512) == 2 and call(hd=4) == 2 and call(hd=264) == 2 and call(hd=0) == 2
     assert call(q=A + 8) == 3 and call(o=4 * A + 2) == 3
     assert call(o=A) == 1  # o overlaps q
     assert call(Sq=2 ** 31 - 100) == 2
@@ -104,7 +108,9 @@ def test_workspace_size_and_errors_without_a_device(fa):
         o_bytes = 512 * 2 * 128 * hd * 4
         ml_bytes = 512 * 2 * 2 * 128 * 4
         assert fa.workspace_bytes(hd) == o_bytes + ml_bytes
-    assert fa.workspace_bytes(80) == 0
+    for hd, kh in ((8, 64), (40, 64), (72, 128), (80, 128), (96, 128), (120, 128)):
+        assert fa.workspace_bytes(hd) == fa.workspace_bytes(kh)  # runs on the next kernel up
+    assert fa.workspace_bytes(84) == 0 and fa.workspace_bytes(192) == 0 and fa.workspace_bytes(256) == 0
     ws = fa.workspace_bytes(128)
     args = (A, 2 * A, 3 * A, 4 * A, 1, 4, 2, 8, 8, 128, 1, 0.1)
     for f in (fa.fa_prefill_ws, fa.fa_prefill_ws_bf16):
@@ -112,7 +118,8 @@ def test_workspace_size_and_errors_without_a_device(fa):
         assert f(*args, 5 * A + 16, ws, 0) == 3       # not 256-byte aligned
         assert f(*args, 5 * A, ws - 1, 0) == 1        # too small
         assert f(A, 2 * A, 3 * A, 4 * A, 0, 4, 2, 8, 8, 128, 1, 0.1, 0, 0, 0) == 0  # empty problem: no-op
-        assert f(A, 2 * A, 3 * A, 4 * A, 1, 4, 2, 8, 8, 96, 1, 0.1, 5 * A, ws, 0) == 2
+        assert f(A, 2 * A, 3 * A, 4 * A, 1, 4, 2, 8, 8, 100, 1, 0.1, 5 * A, ws, 0) == 2
+        assert f(A, 2 * A, 3 * A, 4 * A, 1, 4, 2, 8, 8, 192, 1, 0.1, 5 * A, ws, 0) == 2  # split-KV: heads up to 128
 
 
 def test_static_scratch_entry_point_errors_without_a_device(fa):
@@ -128,7 +135,7 @@ def test_static_scratch_entry_point_errors_without_a_device(fa):
                      a["causal"], a["scale"], bf16, 0)
 
         assert call(q=0) == 1 and call(Hkv=3) == 1 and call(scale=0.0) == 1
-        assert call(hd=96) == 2 and call(q=A + 8) == 3
+        assert call(hd=100) == 2 and call(hd=192) == 2 and call(q=A + 8) == 3
         assert call(B=0) == 0 and call(Sq=0, q=0, o=0) == 0
     assert fa.status_string(7).startswith("FA_ERR_SCRATCH")
 
@@ -161,7 +168,7 @@ def test_kvcache_and_append_errors_without_a_device(fa):
     args = (A, 2 * A, 3 * A, 4 * A, 1, 4, 2, 8)
     assert kc(*args, 9, 8, 128, 1, 0.1, 0, 0, 0, 0) == 1       # kv_len > kv_cap
     assert kc(*args, -1, 8, 128, 1, 0.1, 0, 0, 0, 0) == 1
-    assert kc(*args, 8, 16, 96, 1, 0.1, 0, 0, 0, 0) == 2
+    assert kc(*args, 8, 16, 100, 1, 0.1, 0, 0, 0, 0) == 2
     assert kc(*args, 8, 16, 128, 1, 0.1, 1, 5 * A + 16, 1 << 30, 0) == 3   # workspace not 256-aligned
     assert kc(A, 2 * A, 3 * A, 4 * A, 0, 4, 2, 8, 8, 16, 128, 1, 0.1, 0, 0, 0, 0) == 0  # B = 0
 
@@ -179,7 +186,7 @@ def test_paged_errors_without_a_device(fa):
     assert call(page=64) == 1 and call(page=200) == 1 and call(page=0) == 1   # not a multiple of 128
     assert call(maxp=2) == 1                      # 2 pages of 128 < 300 keys
     assert call(nb=0) == 1 and call(bt=0) == 1 and call(kv_len=-1) == 1
-    assert call(bt=24 * A + 2) == 3 and call(hd=96) == 2
+    assert call(bt=24 * A + 2) == 3 and call(hd=100) == 2 and call(hd=192) == 2  # paged: heads up to 128
     assert call(o=9 * A) == 1                     # o inside the K pool
     assert call(B=0) == 0
 
@@ -189,6 +196,7 @@ def test_ex_entry_point_errors_without_a_device(fa):
     args = (A, 2 * A, 3 * A, 4 * A)
     assert f(*args, 5 * A + 2, 1, 4, 2, 8, 8, 128, 1, 0.1, 0, 0, 0, 0) == 3       # misaligned lse
     assert f(*args, 4 * A, 1, 4, 2, 8, 8, 128, 1, 0.1, 0, 0, 0, 0) == 1           # lse inside o
-    assert f(*args, 0, 1, 4, 2, 8, 8, 96, 1, 0.1, 0, 0, 0, 0) == 2
-    assert f(*args, 0, 1, 4, 2, 8, 8, 256, 1, 0.1, 0, 6 * A, 1 << 30, 0) == 2     # split-KV: hd 64 and 128
+    assert f(*args, 0, 1, 4, 2, 8, 8, 100, 1, 0.1, 0, 0, 0, 0) == 2
+    assert f(*args, 0, 1, 4, 2, 8, 8, 256, 1, 0.1, 0, 6 * A, 1 << 30, 0) == 2     # split-KV: heads up to 128
+    assert f(*args, 0, 1, 4, 2, 8, 8, 136, 1, 0.1, 0, 6 * A, 1 << 30, 0) == 2
     assert f(*args, 0, 0, 4, 2, 8, 8, 128, 1, 0.1, 0, 0, 0, 0) == 0               # B = 0

@@ -208,7 +208,7 @@ def test_errors_are_returned_not_hidden():
     k = torch.randn((1, 8, 2, 128), device="cuda").half()
     o = torch.empty_like(q)
     assert fa.fa_prefill(q, k, k, o, 1, 4, 3, 8, 8, 128, 1, 0.1) == 1      # Hq % Hkv
-    assert fa.fa_prefill(q, k, k, o, 1, 4, 2, 8, 8, 96, 1, 0.1) == 2       # hd
+    assert fa.fa_prefill(q, k, k, o, 1, 4, 2, 8, 8, 100, 1, 0.1) == 2      # hd
     assert fa.fa_prefill(q.data_ptr() + 2, k, k, o, 1, 4, 2, 8, 8, 128, 1, 0.1) == 3  # alignment
     assert fa.fa_prefill(q, k, k, q, 1, 4, 2, 8, 8, 128, 1, 0.1) == 1      # o aliases q
     assert fa.fa_prefill(q, k, k, o, 1, 4, 2, 8, 8, 128, 1, float("inf")) == 1
