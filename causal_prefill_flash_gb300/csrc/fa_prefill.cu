@@ -660,16 +660,13 @@ template <int HD>
 struct SkLayout {
   using L = Layout<HD>;
   // The persistent CTA keeps loading the next segment's K/V while it writes
-  // the previous segment's O, so O cannot be staged in the ring: it goes
-  // through its own 32 KB stage (one 128-row x 64-column 16-bit block per
-  // query tile), paid for with one ring slot at hd 128.
-  static constexpr int NSLOT = HD == 128 ? 4 : 8;
-  static constexpr uint32_t STAGE_BYTES = BM * 128;  // one 64-column block of one tile
-  static constexpr uint32_t OFF_STAGE = L::OFF_RING + NSLOT * L::SLOT_BYTES;
-  // q_full, q_empty, full[NSLOT], empty[NSLOT], s_full[2], p_full[2], o_final[2], drain,
-  // o_staged[2], stage_free[2]
-  static constexpr uint32_t NUM_BARS = 2 + 2 * NSLOT + 2 + 2 + 2 + 1 + 2 + 2;
-  static constexpr uint32_t OFF_BAR = OFF_STAGE + 2 * STAGE_BYTES;
+  // the previous segment's O, so O cannot be staged in the ring: each softmax
+  // thread writes its row straight from registers, and the ring keeps the
+  // one-shot kernel's depth.
+  static constexpr int NSLOT = HD == 128 ? 5 : 8;
+  // q_full, q_empty, full[NSLOT], empty[NSLOT], s_full[2], p_full[2], o_final[2], drain
+  static constexpr uint32_t NUM_BARS = 2 + 2 * NSLOT + 2 + 2 + 2 + 1;
+  static constexpr uint32_t OFF_BAR = L::OFF_RING + NSLOT * L::SLOT_BYTES;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr uint32_t BYTES = OFF_MISC + 16;
   static constexpr uint32_t REQUEST = BYTES + 1024;
@@ -752,9 +749,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto bPfull = [&](int x) { return bar + 8u * (4 + 2 * NSLOT + x); };
   auto bOfinal = [&](int x) { return bar + 8u * (6 + 2 * NSLOT + x); };
   const uint32_t bDrain = bar + 8u * (8 + 2 * NSLOT);
-  auto bOstaged = [&](int x) { return bar + 8u * (9 + 2 * NSLOT + x); };    // a block of O_X is in stage x
-  auto bStageFree = [&](int x) { return bar + 8u * (11 + 2 * NSLOT + x); };  // stage x has been read out
-  const uint32_t sStage = sbase + SL::OFF_STAGE;
   uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + SL::OFF_MISC);
   volatile uint32_t* abort_flag = misc + 1;
 
@@ -778,8 +772,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::mbar_init(bSfull(x), 1);
       ptx::mbar_init(bPfull(x), BM);  // one arrival per softmax thread of tile x
       ptx::mbar_init(bOfinal(x), 1);
-      ptx::mbar_init(bOstaged(x), 4);  // one arrival per softmax warp of tile x
-      ptx::mbar_init(bStageFree(x), 1);
     }
     ptx::mbar_init(bDrain, 1);
     misc[1] = 0u;
@@ -973,44 +965,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const float sl2 = p.sl2;
     int cnt = 0;   // tiles processed (s_full / p_full phases)
     int ocnt = 0;  // segments with tiles of x (o_final phases)
-    int nst = 0;   // 64-column blocks of O_X sent through stage x (o_staged / stage_free phases)
     bool ok = true;
-    // One 64-column block of O_X (this thread's row: 64 values, 32 per half)
-    // into stage x, 128-byte swizzled, then out by one TMA tensor store:
-    // whole-line global writes, rows past Sq clipped by the map.  The block
-    // before it must have been read out of the stage first.
-    const uint32_t stage_row = sStage + x * SL::STAGE_BYTES + r * 128;
-    auto stage_half = [&](int h, const float (&o)[32], float sc) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int ch = h * 4 + e;  // 16-byte chunk of the 128-byte row
-        ptx::st_shared_v4(stage_row + ((ch ^ (r % 8)) * 16), pack2<BF16>(o[8 * e + 0] * sc, o[8 * e + 1] * sc),
-                          pack2<BF16>(o[8 * e + 2] * sc, o[8 * e + 3] * sc),
-                          pack2<BF16>(o[8 * e + 4] * sc, o[8 * e + 5] * sc),
-                          pack2<BF16>(o[8 * e + 6] * sc, o[8 * e + 7] * sc));
-      }
-    };
-    auto stage_wait_free = [&]() -> bool {
-      if (nst == 0) return true;
-      return warp_wait_bar(bStageFree(x), (nst - 1) & 1, abort_flag, p.watchdog_ns, WD_SOFTMAX_O_DONE);
-    };
-    auto stage_send = [&](int cb, int hq_, int q0_, int b_) -> bool {
-      ptx::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bOstaged(x));
-      bool sent = true;
-      if (wq == 0) {
-        sent = warp_wait_bar(bOstaged(x), nst & 1, abort_flag, p.watchdog_ns, WD_SOFTMAX_O_DONE);
-        if (sent && lane == 0) {
-          ptx::tma_store_4d(&tmO, sStage + x * SL::STAGE_BYTES, cb * 64, hq_, q0_, b_);
-          ptx::bulk_commit();
-          ptx::bulk_wait_read0();
-          ptx::mbar_arrive(bStageFree(x));
-        }
-      }
-      ++nst;
-      return sent;
-    };
     for (int u = u_beg, jb = j_beg; ok && in_range(u, jb); ++u, jb = 0) {
       const UnitGeo w = unit_geo(p, u);
       const int je = (u == u_end) ? j_end : w.n;
@@ -1149,31 +1104,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const float Lsum = ntile > 0 ? l : 0.f;
       const float inv_l = (Lsum > 0.f) ? 1.f / Lsum : 0.f;
       if (p.lse && q0 + r < p.Sq) p.lse[(static_cast<size_t>(w.b) * p.Hq + hqx) * p.Sq + q0 + r] = row_lse(M, Lsum);
+      // O / l rounded to 16 bits, from registers straight to the row (the ring
+      // is already filling with the next segment's K/V): whole 32-byte sectors
+      // where the row is 32-byte aligned, up to the head's true width
+      uint32_t orr[HD];
+      if (ntile > 0) {
 #pragma unroll
-      for (int cb = 0; cb < (int)L::KCH; ++cb) {
-        ok = stage_wait_free();
-        if (!ok) break;
+        for (int c = 0; c < HD / 32; ++c) ptx::tmem_ld32(tO + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&orr[c * 32]));
+        ptx::tmem_wait_ld();
+        ptx::reg_fence(orr);
+      } else {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int c = cb * 2 + h;  // 32-column piece
-          float o[32];
-          if (ntile > 0) {
-            uint32_t orr[32];
-            ptx::tmem_ld32(tO + c * 32, orr);
-            ptx::tmem_wait_ld();
-            ptx::reg_fence(orr);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(orr[e]);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = 0.f;
-          }
-          stage_half(h, o, inv_l);
-        }
-        ok = stage_send(cb, hqx, q0, w.b);
-        if (!ok) break;
+        for (int e = 0; e < HD; ++e) orr[e] = 0u;
       }
-      if (!ok) break;
+      if (q0 + r < p.Sq) {
+        uint16_t* orow = p.o + ((static_cast<size_t>(w.b) * p.Sq + q0 + r) * p.Hq + hqx) * p.hd;
+        const bool a32 = (reinterpret_cast<uintptr_t>(orow) & 31u) == 0;
+#pragma unroll
+        for (int g = 0; g < HD / 16; ++g) {
+          if (16 * g >= p.hd) break;
+          uint32_t pk[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            pk[e] = pack2<BF16>(__uint_as_float(orr[16 * g + 2 * e]) * inv_l, __uint_as_float(orr[16 * g + 2 * e + 1]) * inv_l);
+          if (a32 && 16 * g + 16 <= p.hd) {
+            ptx::st_global_v8(orow + 16 * g, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
+          } else {
+            *reinterpret_cast<uint4*>(orow + 16 * g) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            if (16 * g + 8 < p.hd) *reinterpret_cast<uint4*>(orow + 16 * g + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          }
+        }
+      }
     }
   }
 
