@@ -45,6 +45,7 @@ _SIG = {
     "fa_smem_bytes": (ctypes.c_uint, [_I]),
     "fa_debug_status": (_I, []),
     "fa_debug_status_clear": (_I, []),
+    "fa_debug_set_watchdog_ns": (_I, [ctypes.c_ulonglong]),
 }
 
 
@@ -85,6 +86,12 @@ def debug_status() -> int:
 
 def debug_status_clear() -> int:
     return int(load().fa_debug_status_clear())
+
+
+def debug_set_watchdog_ns(ns: int) -> None:
+    """Testing hook: the limit (ns) each pipeline wait of later launches may
+    take before its CTA gives up and reports it (0 restores the 2 s default)."""
+    load().fa_debug_set_watchdog_ns(int(ns))
 
 
 def _ptr(x) -> int:

@@ -85,7 +85,10 @@ static_assert(128 * REGS_CONTROL + 256 * REGS_SOFTMAX <= NUM_THREADS * LAUNCH_RE
               "register split exceeds the launch allocation");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_TAU = 8.0f;  // lazy rescale threshold in log2 units (P <= 2^8)
-constexpr unsigned long long WATCHDOG_NS = 2000000000ull;  // 2 s per wait
+constexpr unsigned long long WATCHDOG_NS = 2000000000ull;  // 2 s per wait (the default; see fa_debug_set_watchdog_ns)
+// Drains wait for work already issued (TMA copies, MMAs), which always
+// completes: their limit is fixed, whatever the wait limit.
+constexpr unsigned long long DRAIN_NS = 2000000000ull;
 
 // Watchdog codes (bits 0-7 of g_fa_status).
 enum : uint32_t {
@@ -204,15 +207,30 @@ __device__ unsigned int g_fa_status = 0;
 __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                        unsigned long long limit_ns, uint32_t code) {
   const uint64_t t0 = ptx::globaltimer_ns();
+  auto give_up = [&]() {
+    *abort_flag = 1u;
+    const uint32_t cta = blockIdx.x < 0xFFFFFFu ? blockIdx.x : 0xFFFFFFu;
+    atomicCAS(&g_fa_status, 0u, (code & 0xFFu) | (cta << 8));
+  };
+  if (limit_ns < 1000000ull) {  // a test making waits run out: the clock after every poll
+    while (!ptx::mbar_try_wait(bar, parity)) {
+      if (*abort_flag) return false;
+      if (ptx::globaltimer_ns() - t0 > limit_ns) {
+        give_up();
+        return false;
+      }
+    }
+    return true;
+  }
+  // try_wait suspends until the phase completes or a hardware time limit, so
+  // the clock is read once per 32 polls
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (ptx::mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
     if (ptx::globaltimer_ns() - t0 > limit_ns) {
-      *abort_flag = 1u;
-      const uint32_t cta = blockIdx.x < 0xFFFFFFu ? blockIdx.x : 0xFFFFFFu;
-      atomicCAS(&g_fa_status, 0u, (code & 0xFFu) | (cta << 8));
+      give_up();
       return false;
     }
   }
@@ -372,13 +390,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ptx::tma_load_4d(sRing + s * L::SLOT_BYTES + c * (BN * 128), m, bFull(s), c * 64, w.hk, row, bat);
         ++issued;
       }
-      if (!ok) {
-        // abort: let every copy already issued land before the CTA exits
-        drain_wait(bQ, 0, p.watchdog_ns);
-        for (int s = 0; s < NSLOT && s < issued; ++s) {
-          const int last = s + NSLOT * ((issued - 1 - s) / NSLOT);
-          drain_wait(bFull(s), (last / NSLOT) & 1, p.watchdog_ns);
-        }
+      // every copy issued has landed before the CTA exits: in a normal run
+      // the MMA thread consumed them all (these waits return at once); in a
+      // CTA that gave up, some may still be in flight
+      drain_wait(bQ, 0, DRAIN_NS);
+      for (int s = 0; s < NSLOT && s < issued; ++s) {
+        const int last = s + NSLOT * ((issued - 1 - s) / NSLOT);
+        drain_wait(bFull(s), (last / NSLOT) & 1, DRAIN_NS);
       }
     }
   } else if (warp == MMA_WARP) {
@@ -442,12 +460,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!ok) break;
         if (more) ptx::mma_commit(bEmpty(sk));
       }
-      if (ok) {
-        ptx::mma_commit(bOfinal);
-      } else {
-        ptx::mma_commit(bDrain);  // completes once every MMA issued above has finished
-        drain_wait(bDrain, 0, p.watchdog_ns);
-      }
+      if (ok) ptx::mma_commit(bOfinal);
+      // every MMA issued has finished before TMEM is freed (the softmax may
+      // have given up without waiting for o_final)
+      ptx::mma_commit(bDrain);
+      drain_wait(bDrain, 0, DRAIN_NS);
     }
   }
   } else {
@@ -860,12 +877,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::tma_load_4d(sRing + s * L::SLOT_BYTES + c * (BN * 128), m, bFull(s), c * 64, w.hk, row, bat);
         }
       }
-      if (!ok) {
-        if (nq > 0) drain_wait(bQfull, (nq - 1) & 1, p.watchdog_ns);
-        for (int s = 0; s < NSLOT && s < g; ++s) {
-          const int last = s + NSLOT * ((g - 1 - s) / NSLOT);
-          drain_wait(bFull(s), (last / NSLOT) & 1, p.watchdog_ns);
-        }
+      // every copy issued has landed before the CTA exits (as in the one-shot kernel)
+      if (nq > 0) drain_wait(bQfull, (nq - 1) & 1, DRAIN_NS);
+      for (int s = 0; s < NSLOT && s < g; ++s) {
+        const int last = s + NSLOT * ((g - 1 - s) / NSLOT);
+        drain_wait(bFull(s), (last / NSLOT) & 1, DRAIN_NS);
       }
     } else if (warp == MMA_WARP && lane == 0) {
       // ------------------------------------------------------- MMA issuer
@@ -947,10 +963,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         cnt1 += nBs;
         ++nq;
       }
-      if (!ok) {
-        ptx::mma_commit(bDrain);
-        drain_wait(bDrain, 0, p.watchdog_ns);
-      }
+      // every MMA issued has finished before TMEM is freed
+      ptx::mma_commit(bDrain);
+      drain_wait(bDrain, 0, DRAIN_NS);
     }
   } else {
     ptx::setmaxnreg_inc<SK_REGS_SOFTMAX>();
@@ -1281,6 +1296,9 @@ static long long unit_count_of(const Params& p) {
 
 constexpr int MAX_DEVICES = 64;
 
+// The wait limit the next launches give their kernels (fa_debug_set_watchdog_ns).
+static std::atomic<unsigned long long> g_watchdog_ns{WATCHDOG_NS};
+
 // Per-device facts, filled once: 1 = sm_103 with enough opt-in shared memory.
 static std::atomic<int> g_dev_ok[MAX_DEVICES];
 static std::atomic<int> g_dev_sms[MAX_DEVICES];
@@ -1413,7 +1431,7 @@ static int launch(const void* q, const void* k, const void* v, void* o, int hd, 
   prm.pair_heads = (prm.G % 2 == 0) ? 1 : 0;
   prm.causal = causal ? 1 : 0;
   prm.sl2 = scale * 1.4426950408889634f;
-  prm.watchdog_ns = WATCHDOG_NS;
+  prm.watchdog_ns = g_watchdog_ns.load();
   const long long grid = grid_size(B, Hq, Hkv, Sq);
   if (launch_pdl(kern, dim3((unsigned)grid), dim3(NUM_THREADS), L::REQUEST, stream, mq, mk, mv, mo, mkt, mvt, prm) !=
       cudaSuccess) {
@@ -1455,7 +1473,7 @@ static int launch256(const void* q, const void* k, const void* v, void* o, int h
   prm.n_qtiles = (Sq + BM - 1) / BM;
   prm.causal = causal ? 1 : 0;
   prm.sl2 = scale * 1.4426950408889634f;
-  prm.watchdog_ns = WATCHDOG_NS;
+  prm.watchdog_ns = g_watchdog_ns.load();
   prm.lse = lse;
   const long long grid = (long long)prm.n_qtiles * Hq * B;
   if (grid > 0x7FFFFFFFLL) return FA_ERR_UNSUPPORTED;
@@ -1710,7 +1728,7 @@ static int launch_sk(const void* q, const void* k, const void* v, void* o, int h
   prm.num_blocks = pkv.num_blocks;
   prm.last_page = pkv.last_page;
   prm.lse = lse;
-  prm.watchdog_ns = WATCHDOG_NS;
+  prm.watchdog_ns = g_watchdog_ns.load();
   SkSchedule sc;
   get_schedule(prm, g_dev_sms[dev].load(), &sc);
   std::memcpy(sp.su, sc.su, sizeof(int) * (sc.G + 1));
@@ -1944,7 +1962,7 @@ static int launch_sk_static(const void* q, const void* k, const void* v, void* o
   prm.pair_heads = (prm.G % 2 == 0) ? 1 : 0;
   prm.causal = causal ? 1 : 0;
   prm.sl2 = scale * 1.4426950408889634f;
-  prm.watchdog_ns = WATCHDOG_NS;
+  prm.watchdog_ns = g_watchdog_ns.load();
   SkSchedule sc;
   get_schedule(prm, g_dev_sms[dev].load(), &sc);
   if (static_bytes_needed(HD, sc.slots) > FA_STATIC_SCRATCH_BYTES) return FA_ERR_SCRATCH;
@@ -2113,5 +2131,10 @@ extern "C" int fa_debug_status_clear(void) {
     (void)cudaGetLastError();
     return FA_ERR_DEVICE;
   }
+  return FA_OK;
+}
+
+extern "C" int fa_debug_set_watchdog_ns(unsigned long long ns) {
+  fa::g_watchdog_ns.store(ns == 0 ? fa::WATCHDOG_NS : ns);
   return FA_OK;
 }

@@ -157,12 +157,11 @@ __global__ void __launch_bounds__(NUM_THREADS_256, 1)
         if (ok) load_half(&tmV, j, 0);
         if (ok) load_half(&tmV, j, 1);
       }
-      if (!ok) {  // abort: let every copy already issued land before the CTA exits
-        drain_wait(bQ, 0, p.watchdog_ns);
-        for (int s = 0; s < NSLOT && s < g; ++s) {
-          const int last = s + NSLOT * ((g - 1 - s) / NSLOT);
-          drain_wait(bFull(s), (last / NSLOT) & 1, p.watchdog_ns);
-        }
+      // every copy issued has landed before the CTA exits (as in the two-tile kernel)
+      drain_wait(bQ, 0, DRAIN_NS);
+      for (int s = 0; s < NSLOT && s < g; ++s) {
+        const int last = s + NSLOT * ((g - 1 - s) / NSLOT);
+        drain_wait(bFull(s), (last / NSLOT) & 1, DRAIN_NS);
       }
     }
   } else if (warp == MMA_WARP_256) {
@@ -223,12 +222,9 @@ __global__ void __launch_bounds__(NUM_THREADS_256, 1)
         if (!ok) break;
         issue_pv(j > 0);
       }
-      if (ok) {
-        ptx::mma_commit(bOfinal);
-      } else {
-        ptx::mma_commit(bDrain);
-        drain_wait(bDrain, 0, p.watchdog_ns);
-      }
+      if (ok) ptx::mma_commit(bOfinal);
+      ptx::mma_commit(bDrain);  // every MMA issued has finished before TMEM is freed
+      drain_wait(bDrain, 0, DRAIN_NS);
     }
   } else if (warp < 4) {
     // -------------------------------------------------------------- softmax

@@ -77,6 +77,7 @@
  *   fa_kv_append                     write new tokens' K/V rows into a cache
  *   fa_prefill_ws_static             split-KV with library-owned scratch
  *   fa_status_string, fa_smem_bytes, fa_debug_status(_clear)  diagnostics
+ *   fa_debug_set_watchdog_ns         testing hook: the kernels' wait limit
  */
 #ifndef FA_PREFILL_H
 #define FA_PREFILL_H
@@ -374,6 +375,18 @@ int fa_debug_status(void);
 
 /* Reset the watchdog word of the current device to 0 (synchronous). Returns an fa_status_t. */
 int fa_debug_status_clear(void);
+
+/*
+ * fa_debug_set_watchdog_ns -- a testing hook: the limit, in nanoseconds, that
+ * each pipeline wait of the kernels launched after this call may take before
+ * its CTA gives up (default 2 s; 0 restores it).  A tiny limit makes waits run
+ * out on purpose, so a test can check that a CTA which gives up records its
+ * code in the watchdog word, waits for the copies and MMAs it already issued,
+ * frees its TMEM and exits, and that the context stays usable.  The output of
+ * a call whose CTAs gave up is undefined.  Host-only (no device call);
+ * process-wide.  Returns FA_OK.
+ */
+int fa_debug_set_watchdog_ns(unsigned long long ns);
 
 #ifdef __cplusplus
 }
