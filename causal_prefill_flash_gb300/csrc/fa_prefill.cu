@@ -202,51 +202,62 @@ __device__ __forceinline__ int kv_tiles(const Params& p, int q0, bool has) {
 
 __device__ unsigned int g_fa_status = 0;
 
+__device__ __forceinline__ void give_up_wait(volatile uint32_t* abort_flag, uint32_t code) {
+  *abort_flag = 1u;
+  const uint32_t cta = blockIdx.x < 0xFFFFFFu ? blockIdx.x : 0xFFFFFFu;
+  atomicCAS(&g_fa_status, 0u, (code & 0xFFu) | (cta << 8));
+}
+
 // Slow path of a bounded wait: poll, then give up after the watchdog limit
-// (or as soon as another role of this CTA has given up).
+// (or as soon as another role of this CTA has given up).  try_wait suspends
+// until the phase completes or a hardware time limit, so the clock is read
+// once per 32 polls; under a limit below 1 ms (a test making waits run out)
+// it is read after every poll.  Two codings of that test path, chosen per
+// kernel by measurement (the code around the normal loop changes how the
+// kernels around it compile): kSeparate, a loop of its own (the two-tile and
+// stream-K kernels), or an early exit from the normal loop (the hd 256 kernel).
+template <bool kSeparate = true>
 __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                       unsigned long long limit_ns, uint32_t code) {
+                                          unsigned long long limit_ns, uint32_t code) {
   const uint64_t t0 = ptx::globaltimer_ns();
-  auto give_up = [&]() {
-    *abort_flag = 1u;
-    const uint32_t cta = blockIdx.x < 0xFFFFFFu ? blockIdx.x : 0xFFFFFFu;
-    atomicCAS(&g_fa_status, 0u, (code & 0xFFu) | (cta << 8));
-  };
-  if (limit_ns < 1000000ull) {  // a test making waits run out: the clock after every poll
+  const bool fine = limit_ns < 1000000ull;
+  if (kSeparate && fine) {
     while (!ptx::mbar_try_wait(bar, parity)) {
       if (*abort_flag) return false;
       if (ptx::globaltimer_ns() - t0 > limit_ns) {
-        give_up();
+        give_up_wait(abort_flag, code);
         return false;
       }
     }
     return true;
   }
-  // try_wait suspends until the phase completes or a hardware time limit, so
-  // the clock is read once per 32 polls
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i)
+    for (int i = 0; i < 32; ++i) {
       if (ptx::mbar_try_wait(bar, parity)) return true;
+      if (!kSeparate && fine) break;
+    }
     if (*abort_flag) return false;
     if (ptx::globaltimer_ns() - t0 > limit_ns) {
-      give_up();
+      give_up_wait(abort_flag, code);
       return false;
     }
   }
 }
 
+template <bool kSeparate = true>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                          unsigned long long limit_ns, uint32_t code) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
-  return wait_slow(bar, parity, abort_flag, limit_ns, code);
+  return wait_slow<kSeparate>(bar, parity, abort_flag, limit_ns, code);
 }
 
 // Warp-uniform bounded wait (all 32 lanes call it; all get the same answer).
+template <bool kSeparate = true>
 __device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity,
                                               volatile uint32_t* abort_flag,
                                               unsigned long long limit_ns, uint32_t code) {
-  const bool ok = wait_bar(bar, parity, abort_flag, limit_ns, code);
+  const bool ok = wait_bar<kSeparate>(bar, parity, abort_flag, limit_ns, code);
   return __all_sync(0xffffffffu, ok);
 }
 

@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(NUM_THREADS_256, 1)
       bool ok = true;
       auto load_half = [&](const CUtensorMap* m, int t, int h) {
         const int s = g % NSLOT;
-        if (g >= NSLOT) ok = wait_bar(bEmpty(s), ((g / NSLOT) & 1) ^ 1u, abort_flag, p.watchdog_ns, WD_PRODUCER_EMPTY);
+        if (g >= NSLOT) ok = wait_bar<false>(bEmpty(s), ((g / NSLOT) & 1) ^ 1u, abort_flag, p.watchdog_ns, WD_PRODUCER_EMPTY);
         if (!ok) return;
         ptx::mbar_arrive_expect_tx(bFull(s), L::HALF_BYTES);
 #pragma unroll
@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(NUM_THREADS_256, 1)
       bool ok = true;
       auto half_ready = [&]() -> int {
         const int s = g % NSLOT;
-        ok = wait_bar(bFull(s), (g / NSLOT) & 1, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);
+        ok = wait_bar<false>(bFull(s), (g / NSLOT) & 1, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);
         return s;
       };
       auto issue_s = [&]() {  // S = Q K^T over both hd halves, slot by slot
@@ -209,16 +209,16 @@ __global__ void __launch_bounds__(NUM_THREADS_256, 1)
         }
         if (ok) ptx::mma_commit(bPVdone);
       };
-      ok = wait_bar(bQ, 0, abort_flag, p.watchdog_ns, WD_MMA_Q);
+      ok = wait_bar<false>(bQ, 0, abort_flag, p.watchdog_ns, WD_MMA_Q);
       if (ok && n > 0) issue_s();
       for (int j = 0; ok && j < n; ++j) {
         if (j + 1 < n) {  // S(j+1) once the softmax holds S(j) in registers
-          ok = wait_bar(bSfree, j & 1, abort_flag, p.watchdog_ns, WD_MMA_P_FULL);
+          ok = wait_bar<false>(bSfree, j & 1, abort_flag, p.watchdog_ns, WD_MMA_P_FULL);
           if (!ok) break;
           issue_s();
           if (!ok) break;
         }
-        ok = wait_bar(bPfull, j & 1, abort_flag, p.watchdog_ns, WD_MMA_P_FULL);
+        ok = wait_bar<false>(bPfull, j & 1, abort_flag, p.watchdog_ns, WD_MMA_P_FULL);
         if (!ok) break;
         issue_pv(j > 0);
       }
@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(NUM_THREADS_256, 1)
     float l = 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
-      ok = warp_wait_bar(bSfull, j & 1, abort_flag, p.watchdog_ns, WD_SOFTMAX_S_FULL);
+      ok = warp_wait_bar<false>(bSfull, j & 1, abort_flag, p.watchdog_ns, WD_SOFTMAX_S_FULL);
       if (!ok) break;
       ptx::tc_fence_after();
       uint32_t sr[BN];
@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(NUM_THREADS_256, 1)
         l += a0 + a1;
       }
       if (j > 0) {  // P(j-1) consumed and O updated before P(j) and a rescale
-        ok = warp_wait_bar(bPVdone, (j - 1) & 1, abort_flag, p.watchdog_ns, WD_SOFTMAX_O_DONE);
+        ok = warp_wait_bar<false>(bPVdone, (j - 1) & 1, abort_flag, p.watchdog_ns, WD_SOFTMAX_O_DONE);
         if (!ok) break;
         ptx::tc_fence_after();
         if (__any_sync(0xffffffffu, resc)) {
@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(NUM_THREADS_256, 1)
     // After o_final every half tile loaded was consumed: ring slots 0 and 1
     // (64 KB, contiguous) stage O, written out by one TMA store per 64 columns.
     if (ok && n > 0) {
-      ok = warp_wait_bar(bOfinal, 0, abort_flag, p.watchdog_ns, WD_SOFTMAX_O_DONE);
+      ok = warp_wait_bar<false>(bOfinal, 0, abort_flag, p.watchdog_ns, WD_SOFTMAX_O_DONE);
       if (ok) ptx::tc_fence_after();
     }
     if (ok) {
@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(NUM_THREADS_256, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bOstaged);
       if (warp == 0) {
-        ok = warp_wait_bar(bOstaged, 0, abort_flag, p.watchdog_ns, WD_SOFTMAX_O_DONE);
+        ok = warp_wait_bar<false>(bOstaged, 0, abort_flag, p.watchdog_ns, WD_SOFTMAX_O_DONE);
         if (ok && lane == 0) {
 #pragma unroll
           for (int c = 0; c < (int)L::KCH; ++c)  // a narrower head has no columns past p.hd: no store there
