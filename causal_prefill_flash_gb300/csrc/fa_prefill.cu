@@ -415,25 +415,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t IDESC_S = ptx::idesc_f16(BF16, BM, BN, false, false);  // Q, K both K-major
       constexpr uint32_t IDESC_O = ptx::idesc_f16(BF16, BM, HD, false, true);   // P from TMEM, V MN-major
+      constexpr uint32_t DHI = ptx::sdesc_sw128_hi(1024);  // Q, K (K-major) and V (MN-major): SBO 1024
       auto issue_s = [&](int x, int slot) {
         const uint32_t d = tmem + L::TM_S + x * BN;
-        const uint32_t q = sQ + x * L::Q_BYTES;
-        const uint32_t k = sRing + slot * L::SLOT_BYTES;
+        const uint32_t q = ptx::sdesc_sw128_lo(sQ + x * L::Q_BYTES, 16);
+        const uint32_t k = ptx::sdesc_sw128_lo(sRing + slot * L::SLOT_BYTES, 16);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t o = (kk / 4) * (BM * 128) + (kk % 4) * 32;
-          ptx::mma_f16_ss(d, ptx::sdesc_sw128(q + o, 16, 1024), ptx::sdesc_sw128(k + o, 16, 1024), IDESC_S,
-                          kk > 0 ? 1u : 0u);
+          const uint32_t o = ((kk / 4) * (BM * 128) + (kk % 4) * 32) >> 4;
+          ptx::mma_f16_ss(d, ptx::sdesc_join(q + o, DHI), ptx::sdesc_join(k + o, DHI), IDESC_S, kk > 0 ? 1u : 0u);
         }
         ptx::mma_commit(bSfull(x));
       };
       auto issue_pv = [&](int x, int slot, bool acc) {
         const uint32_t d = tmem + L::TM_O + x * HD;
         const uint32_t a = tmem + L::TM_S + x * BN;  // P_X, 2 elements per column
-        const uint32_t v = sRing + slot * L::SLOT_BYTES;
+        const uint32_t v = ptx::sdesc_sw128_lo(sRing + slot * L::SLOT_BYTES, BN * 128);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          ptx::mma_f16_ts(d, a + kk * 8, ptx::sdesc_sw128(v + kk * (16 * 128), BN * 128, 1024), IDESC_O,
+          ptx::mma_f16_ts(d, a + kk * 8, ptx::sdesc_join(v + kk * ((16 * 128) >> 4), DHI), IDESC_O,
                           (acc || kk > 0) ? 1u : 0u);
       };
       bool ok = wait_bar(bQ, 0, abort_flag, p.watchdog_ns, WD_MMA_Q);
@@ -898,25 +898,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ------------------------------------------------------- MMA issuer
       constexpr uint32_t IDESC_S = ptx::idesc_f16(BF16, BM, BN, false, false);
       constexpr uint32_t IDESC_O = ptx::idesc_f16(BF16, BM, HD, false, true);
+      constexpr uint32_t DHI = ptx::sdesc_sw128_hi(1024);  // Q, K (K-major) and V (MN-major): SBO 1024
       auto issue_s = [&](int x, int slot) {
         const uint32_t d = tmem + L::TM_S + x * BN;
-        const uint32_t q = sQ + x * L::Q_BYTES;
-        const uint32_t k = sRing + slot * L::SLOT_BYTES;
+        const uint32_t q = ptx::sdesc_sw128_lo(sQ + x * L::Q_BYTES, 16);
+        const uint32_t k = ptx::sdesc_sw128_lo(sRing + slot * L::SLOT_BYTES, 16);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t o = (kk / 4) * (BM * 128) + (kk % 4) * 32;
-          ptx::mma_f16_ss(d, ptx::sdesc_sw128(q + o, 16, 1024), ptx::sdesc_sw128(k + o, 16, 1024), IDESC_S,
-                          kk > 0 ? 1u : 0u);
+          const uint32_t o = ((kk / 4) * (BM * 128) + (kk % 4) * 32) >> 4;
+          ptx::mma_f16_ss(d, ptx::sdesc_join(q + o, DHI), ptx::sdesc_join(k + o, DHI), IDESC_S, kk > 0 ? 1u : 0u);
         }
         ptx::mma_commit(bSfull(x));
       };
       auto issue_pv = [&](int x, int slot, bool acc) {
         const uint32_t d = tmem + L::TM_O + x * HD;
         const uint32_t a = tmem + L::TM_S + x * BN;
-        const uint32_t v = sRing + slot * L::SLOT_BYTES;
+        const uint32_t v = ptx::sdesc_sw128_lo(sRing + slot * L::SLOT_BYTES, BN * 128);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          ptx::mma_f16_ts(d, a + kk * 8, ptx::sdesc_sw128(v + kk * (16 * 128), BN * 128, 1024), IDESC_O,
+          ptx::mma_f16_ts(d, a + kk * 8, ptx::sdesc_join(v + kk * ((16 * 128) >> 4), DHI), IDESC_O,
                           (acc || kk > 0) ? 1u : 0u);
       };
       int g = 0, nq = 0, cnt0 = 0, cnt1 = 0;

@@ -169,6 +169,7 @@ __global__ void __launch_bounds__(NUM_THREADS_256, 1)
     if (lane == 0) {
       constexpr uint32_t IDESC_S = ptx::idesc_f16(BF16, BM, BN, false, false);   // Q, K both K-major
       constexpr uint32_t IDESC_O = ptx::idesc_f16(BF16, BM, 128, false, true);   // P from TMEM, V MN-major
+      constexpr uint32_t DHI = ptx::sdesc_sw128_hi(1024);  // Q, K (K-major) and V (MN-major): SBO 1024
       int g = 0;  // half tiles consumed, in load order
       bool ok = true;
       auto half_ready = [&]() -> int {
@@ -181,13 +182,14 @@ __global__ void __launch_bounds__(NUM_THREADS_256, 1)
           const int s = half_ready();
           if (!ok) return;
           ptx::tc_fence_after();
-          const uint32_t k = sRing + s * L::HALF_BYTES;
+          const uint32_t q = ptx::sdesc_sw128_lo(sQ, 16);
+          const uint32_t k = ptx::sdesc_sw128_lo(sRing + s * L::HALF_BYTES, 16);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {  // 16 hd columns per MMA
-            const uint32_t oq = (2 * h + kk / 4) * (BM * 128) + (kk % 4) * 32;
-            const uint32_t ok_ = (kk / 4) * (BN * 128) + (kk % 4) * 32;
-            ptx::mma_f16_ss(tmem + L::TM_S, ptx::sdesc_sw128(sQ + oq, 16, 1024), ptx::sdesc_sw128(k + ok_, 16, 1024),
-                            IDESC_S, (h > 0 || kk > 0) ? 1u : 0u);
+            const uint32_t oq = ((2 * h + kk / 4) * (BM * 128) + (kk % 4) * 32) >> 4;
+            const uint32_t ok_ = ((kk / 4) * (BN * 128) + (kk % 4) * 32) >> 4;
+            ptx::mma_f16_ss(tmem + L::TM_S, ptx::sdesc_join(q + oq, DHI), ptx::sdesc_join(k + ok_, DHI), IDESC_S,
+                            (h > 0 || kk > 0) ? 1u : 0u);
           }
           ptx::mma_commit(bEmpty(s));
           ++g;
@@ -199,11 +201,11 @@ __global__ void __launch_bounds__(NUM_THREADS_256, 1)
           const int s = half_ready();
           if (!ok) return;
           ptx::tc_fence_after();
-          const uint32_t v = sRing + s * L::HALF_BYTES;
+          const uint32_t v = ptx::sdesc_sw128_lo(sRing + s * L::HALF_BYTES, BN * 128);
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
             ptx::mma_f16_ts(tmem + L::TM_O + h * 128, tmem + L::TM_P + kk * 8,
-                            ptx::sdesc_sw128(v + kk * (16 * 128), BN * 128, 1024), IDESC_O, (acc || kk > 0) ? 1u : 0u);
+                            ptx::sdesc_join(v + kk * ((16 * 128) >> 4), DHI), IDESC_O, (acc || kk > 0) ? 1u : 0u);
           ptx::mma_commit(bEmpty(s));
           ++g;
         }

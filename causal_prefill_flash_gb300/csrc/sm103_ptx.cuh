@@ -262,6 +262,24 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
+// The same descriptor as two 32-bit words.  The high word (SBO, version,
+// layout) is shared by every tile of one layout; the low word is the start
+// address >> 4 plus LBO >> 4 in bits 16-29.  Shared-memory addresses stay
+// below 256 KB, so the address field never carries into bit 14: the
+// descriptor of an address `off` bytes further (off a multiple of 16) is the
+// low word plus off >> 4.  Inside the MMA issuing loop that is one 32-bit add
+// per operand instead of a 64-bit one, and the issuing thread's instruction
+// count per MMA sets its pace.
+__device__ __forceinline__ uint32_t sdesc_sw128_lo(uint32_t saddr, uint32_t lbo_bytes) {
+  return (saddr >> 4) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t sdesc_sw128_hi(uint32_t sbo_bytes) {
+  return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+__device__ __forceinline__ uint64_t sdesc_join(uint32_t lo, uint32_t hi) {
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
 // Instruction descriptor, kind::f16 with an f32 accumulator:
 //   bits 4-5 D type (1 = f32); bits 7-9 A type, 10-12 B type (0 = f16, 1 = bf16);
 //   bit 15 A major, bit 16 B major (0 = K-major, 1 = MN-major);
