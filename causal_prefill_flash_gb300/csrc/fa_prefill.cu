@@ -115,7 +115,8 @@ struct Layout {
   static constexpr uint32_t OFF_Q = 0;               // Q_A, Q_B
   static constexpr uint32_t OFF_RING = 2 * Q_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_RING + NSLOT * SLOT_BYTES;
-  // q_full, full[NSLOT], empty[NSLOT], s_full[2], p_full[2], o_final, drain, o_staged[2]
+  // q_full (Q and K_0), pair[NPB <= NSLOT] (V_j, K_j+1), empty[NSLOT], s_full[2], p_full[2], o_final,
+  // drain, o_staged[2]
   static constexpr uint32_t NUM_BARS = 1 + 2 * NSLOT + 2 + 2 + 2 + 2;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
   static constexpr uint32_t BYTES = OFF_MISC + 16;
@@ -291,6 +292,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                       const Params p) {
   using L = Layout<HD>;
   constexpr int NSLOT = L::NSLOT;
+  // K/V arrive in pairs (V_j, K_j+1) on one barrier, so the MMA thread waits
+  // once per KV step; K_0 arrives with Q.  Pair j+NPB reuses pair j's
+  // barrier.  The producer arms it only once pair j has completed, and with
+  // 2 NPB >= NSLOT it cannot complete before the MMA thread has waited for
+  // pair j: its V's ring slot is freed only by P V(j) or a later MMA.
+  constexpr int NPB = (NSLOT + 1) / 2;
+  static_assert(2 * NPB >= NSLOT && NPB <= NSLOT, "pair barriers");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -300,7 +308,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t sRing = sbase + L::OFF_RING;
   const uint32_t bar = sbase + L::OFF_BAR;
   const uint32_t bQ = bar;
-  auto bFull = [&](int s) { return bar + 8u * (1 + s); };
+  auto bPair = [&](int b) { return bar + 8u * (1 + b); };  // b < NPB
   auto bEmpty = [&](int s) { return bar + 8u * (1 + NSLOT + s); };
   auto bSfull = [&](int x) { return bar + 8u * (1 + 2 * NSLOT + x); };
   auto bPfull = [&](int x) { return bar + 8u * (3 + 2 * NSLOT + x); };
@@ -320,10 +328,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bQ, 1);
-    for (int s = 0; s < NSLOT; ++s) {
-      ptx::mbar_init(bFull(s), 1);
-      ptx::mbar_init(bEmpty(s), 1);
-    }
+    for (int b = 0; b < NPB; ++b) ptx::mbar_init(bPair(b), 2);  // one arrival per load of the pair
+    for (int s = 0; s < NSLOT; ++s) ptx::mbar_init(bEmpty(s), 1);
     for (int x = 0; x < 2; ++x) {
       ptx::mbar_init(bSfull(x), 1);
       ptx::mbar_init(bPfull(x), BM);  // one arrival per softmax thread of tile x
@@ -357,7 +363,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::prefetch_tmap(&tmK);
       ptx::prefetch_tmap(&tmV);
       ptx::prefetch_tmap(&tmO);
-      ptx::mbar_arrive_expect_tx(bQ, L::Q_BYTES * (w.has[1] ? 2u : 1u));
+      ptx::mbar_arrive_expect_tx(bQ, L::Q_BYTES * (w.has[1] ? 2u : 1u) + (n > 0 ? L::SLOT_BYTES : 0u));
       for (int x = 0; x < 2; ++x) {
         if (!w.has[x]) continue;
 #pragma unroll
@@ -365,6 +371,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ptx::tma_load_4d(sQ + x * L::Q_BYTES + c * (BM * 128), &tmQ, bQ, c * 64, w.hq[x], w.q0[x], w.b);
       }
       // loads in order K_0, V_0, K_1, V_1, ...; load i goes to slot i % NSLOT
+      // (K_0 on bQ, then V_j and K_j+1 on pair barrier j % NPB)
       int issued = 0;
       bool ok = true;
       int page = -1, blk = 0;  // paged K/V: the pool block of the current page
@@ -394,20 +401,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           bat = blk;
           tail = pg == p.last_page;
         }
-        ptx::mbar_arrive_expect_tx(bFull(s), L::SLOT_BYTES);
+        const int pj = (i - 1) >> 1;  // pair of load i (V_pj, K_pj+1)
+        const uint32_t fb = i == 0 ? bQ : bPair(pj % NPB);
+        // pair pj reuses pair pj-NPB's barrier: that phase must have completed
+        if ((i & 1) && pj >= NPB) ok = wait_bar(fb, ((pj - NPB) / NPB) & 1, abort_flag, p.watchdog_ns, WD_PRODUCER_EMPTY);
+        if (!ok) break;
+        if (i > 0) ptx::mbar_arrive_expect_tx(fb, L::SLOT_BYTES);
         const CUtensorMap* m = (i & 1) ? (tail ? &tmVt : &tmV) : (tail ? &tmKt : &tmK);
 #pragma unroll
         for (int c = 0; c < (int)L::KCH; ++c)
-          ptx::tma_load_4d(sRing + s * L::SLOT_BYTES + c * (BN * 128), m, bFull(s), c * 64, w.hk, row, bat);
+          ptx::tma_load_4d(sRing + s * L::SLOT_BYTES + c * (BN * 128), m, fb, c * 64, w.hk, row, bat);
         ++issued;
       }
+      // a pair whose K was not issued (the last V, or a CTA that gave up):
+      // its second arrival without bytes
+      if (issued >= 2 && (issued & 1) == 0) ptx::mbar_arrive(bPair(((issued - 2) >> 1) % NPB));
       // every copy issued has landed before the CTA exits: in a normal run
       // the MMA thread consumed them all (these waits return at once); in a
       // CTA that gave up, some may still be in flight
       drain_wait(bQ, 0, DRAIN_NS);
-      for (int s = 0; s < NSLOT && s < issued; ++s) {
-        const int last = s + NSLOT * ((issued - 1 - s) / NSLOT);
-        drain_wait(bFull(s), (last / NSLOT) & 1, DRAIN_NS);
+      const int npairs = issued / 2;  // pairs armed
+      for (int b = 0; b < NPB && b < npairs; ++b) {
+        const int last = b + NPB * ((npairs - 1 - b) / NPB);
+        drain_wait(bPair(b), (last / NPB) & 1, DRAIN_NS);
       }
     }
   } else if (warp == MMA_WARP) {
@@ -436,26 +452,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ptx::mma_f16_ts(d, a + kk * 8, ptx::sdesc_join(v + kk * ((16 * 128) >> 4), DHI), IDESC_O,
                           (acc || kk > 0) ? 1u : 0u);
       };
-      bool ok = wait_bar(bQ, 0, abort_flag, p.watchdog_ns, WD_MMA_Q);
+      bool ok = wait_bar(bQ, 0, abort_flag, p.watchdog_ns, WD_MMA_Q);  // Q and K_0
       if (ok && n > 0) {
-        ok = wait_bar(bFull(0), 0, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);
-        if (ok) {
-          ptx::tc_fence_after();
-          if (nA > 0) issue_s(0, 0);
-          if (nB > 0) issue_s(1, 0);
-          ptx::mma_commit(bEmpty(0));
-        }
+        ptx::tc_fence_after();
+        if (nA > 0) issue_s(0, 0);
+        if (nB > 0) issue_s(1, 0);
+        ptx::mma_commit(bEmpty(0));
       }
       for (int j = 0; ok && j < n; ++j) {
         const int iv = 2 * j + 1, sv = iv % NSLOT;  // V_j
         const int ik = 2 * j + 2, sk = ik % NSLOT;  // K_{j+1}
         const bool more = j + 1 < n;
-        ok = wait_bar(bFull(sv), (iv / NSLOT) & 1, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);
+        ok = wait_bar(bPair(j % NPB), (j / NPB) & 1, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);  // V_j, K_{j+1}
         if (!ok) break;
-        if (more) {
-          ok = wait_bar(bFull(sk), (ik / NSLOT) & 1, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);
-          if (!ok) break;
-        }
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
           const int nX = x == 0 ? nA : nB;
