@@ -760,7 +760,7 @@ __host__ __device__ __forceinline__ UnitGeo unit_geo(const Params& p, int u) {
   return w;
 }
 
-template <int HD, bool BF16>
+template <int HD, bool BF16, bool ONE_SEG>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fa_prefill_sk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -930,7 +930,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       };
       int g = 0, nq = 0, cnt0 = 0, cnt1 = 0;
       bool ok = true;
-      for (int u = u_beg, jb = j_beg; ok && in_range(u, jb); ++u, jb = 0) {
+      // With one segment per CTA the loop runs once, and the compiler lays
+      // out the step loop as in the one-shot kernel (measured: the nested
+      // form issues ~15 % slower).
+      for (int u = u_beg, jb = j_beg; ok && (ONE_SEG ? u == u_beg : in_range(u, jb)); ++u, jb = 0) {
         const UnitGeo w = unit_geo(p, u);
         const int je = (u == u_end) ? j_end : w.n;
         if (je <= jb) continue;
@@ -1323,7 +1326,7 @@ static std::atomic<unsigned long long> g_watchdog_ns{WATCHDOG_NS};
 static std::atomic<int> g_dev_ok[MAX_DEVICES];
 static std::atomic<int> g_dev_sms[MAX_DEVICES];
 static std::atomic<int> g_attr_set[MAX_DEVICES][4];
-static std::atomic<int> g_sk_attr_set[MAX_DEVICES][4];
+static std::atomic<int> g_sk_attr_set[MAX_DEVICES][8];
 static std::atomic<int> g_attr256_set[MAX_DEVICES][2];
 
 static int check_device(int* dev_out) {
@@ -1584,6 +1587,7 @@ struct SkSchedule {
   short ph[SK_MAX_CTAS];
   int slots;    // piece slots in use
   int n_split;  // split pairs
+  int one_seg;  // every CTA runs exactly one segment
   int mu[SK_MAX_CTAS];
   short ms[SK_MAX_CTAS];
   short mn[SK_MAX_CTAS];
@@ -1601,6 +1605,37 @@ static int g_sched_n = 0, g_sched_next = 0;
 constexpr int SK_SEG_COST_Q = 8;  // fixed cost of a segment: two KV steps
 constexpr int SK_MIN_PIECE = 2;
 
+// Pieces of one pair per CTA (as many pairs as CTAs or fewer): pair u is cut
+// into k_u pieces of near-equal length, the next CTA always going to the pair
+// whose pieces are longest, and no piece is shorter than SK_MIN_PIECE steps.
+// Every CTA then runs a single segment.
+static int pieces_schedule(const std::vector<int>& n, int gmax, SkSchedule* sc) {
+  const int nu = static_cast<int>(n.size());
+  std::vector<int> k(static_cast<size_t>(nu), 1);
+  for (int left = gmax - nu; left > 0; --left) {
+    int best = -1;
+    long long best_len = -1;
+    for (int u = 0; u < nu; ++u) {
+      if (n[u] / (k[u] + 1) < SK_MIN_PIECE) continue;
+      const long long len = (n[u] + k[u] - 1) / k[u];
+      if (len > best_len) {
+        best_len = len;
+        best = u;
+      }
+    }
+    if (best < 0) break;
+    ++k[best];
+  }
+  int G = 0;
+  for (int u = 0; u < nu; ++u)
+    for (int i = 0; i < k[u]; ++i) {
+      sc->su[G] = u;
+      sc->sj[G] = static_cast<int>(static_cast<long long>(n[u]) * i / k[u]);
+      ++G;
+    }
+  return G;
+}
+
 static void make_schedule(const Params& prm, int sms, SkSchedule* sc) {
   const long long nu = unit_count_of(prm);
   std::vector<int> n(static_cast<size_t>(nu));
@@ -1609,15 +1644,18 @@ static void make_schedule(const Params& prm, int sms, SkSchedule* sc) {
     n[u] = unit_geo(prm, static_cast<int>(u)).n;
     T += 4LL * n[u] + SK_SEG_COST_Q;
   }
-  const int want = static_cast<int>(std::max<long long>(1, std::min<long long>(std::min(sms, SK_MAX_CTAS), nu * 64)));
-  // CTA c starts at cost T c / want, rounded to a (unit, step) boundary;
-  // boundaries strictly increase, so no CTA's range is empty
+  const int gmax = std::max(1, std::min(sms, SK_MAX_CTAS));
+  const int want = static_cast<int>(std::max<long long>(1, std::min<long long>(gmax, nu * 64)));
   int G = 1;
   sc->su[0] = 0;
   sc->sj[0] = 0;
+  sc->one_seg = nu <= gmax ? 1 : 0;
+  if (sc->one_seg) G = pieces_schedule(n, gmax, sc);
+  // otherwise CTA c starts at cost T c / want, rounded to a (unit, step)
+  // boundary; boundaries strictly increase, so no CTA's range is empty
   long long acc = 0;  // cost of units [0, u)
   int u = 0;
-  for (int c = 1; c < want; ++c) {
+  for (int c = 1; !sc->one_seg && c < want; ++c) {
     const long long target = T * c / want;
     while (u < nu && acc + 4LL * n[u] + SK_SEG_COST_Q <= target) acc += 4LL * n[u++] + SK_SEG_COST_Q;
     if (u >= nu) break;
@@ -1706,20 +1744,23 @@ static int launch_merge(const SkSchedule& sc, const Params& prm, const float4* w
   return FA_OK;
 }
 
+// Opt one stream-K instantiation in to its shared memory, once per device.
+template <typename K>
+static bool sk_attr(K kern, int dev, int slot, uint32_t bytes) {
+  if (g_sk_attr_set[dev][slot].load() != 0) return true;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  g_sk_attr_set[dev][slot].store(1);
+  return true;
+}
+
 template <int HD, bool BF16>
 static int launch_sk(const void* q, const void* k, const void* v, void* o, int hd, int B, int Hq, int Hkv, int Sq, int Skv,
                      int kv_cap, int causal, float scale, void* ws, cudaStream_t stream, int dev,
                      const Paged* pg = nullptr, float* lse = nullptr) {
   using SL = SkLayout<HD>;
-  auto kern = fa_prefill_sk_kernel<HD, BF16>;
-  const int slot = (HD == 128 ? 2 : 0) + (BF16 ? 1 : 0);
-  if (g_sk_attr_set[dev][slot].load() == 0) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SL::REQUEST) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return FA_ERR_SMEM;
-    }
-    g_sk_attr_set[dev][slot].store(1);
-  }
   EncodeTiledFn enc = encoder();
   if (!enc) return FA_ERR_LAUNCH;
   CUtensorMap mq, mk, mv, mo, mkt, mvt;
@@ -1751,6 +1792,8 @@ static int launch_sk(const void* q, const void* k, const void* v, void* o, int h
   prm.watchdog_ns = g_watchdog_ns.load();
   SkSchedule sc;
   get_schedule(prm, g_dev_sms[dev].load(), &sc);
+  auto kern = sc.one_seg ? fa_prefill_sk_kernel<HD, BF16, true> : fa_prefill_sk_kernel<HD, BF16, false>;
+  if (!sk_attr(kern, dev, (HD == 128 ? 2 : 0) + (BF16 ? 1 : 0) + (sc.one_seg ? 4 : 0), SL::REQUEST)) return FA_ERR_SMEM;
   std::memcpy(sp.su, sc.su, sizeof(int) * (sc.G + 1));
   std::memcpy(sp.sj, sc.sj, sizeof(int) * (sc.G + 1));
   std::memcpy(sp.pf, sc.pf, sizeof(short) * sc.G);
@@ -1966,7 +2009,6 @@ static int launch_sk_static(const void* q, const void* k, const void* v, void* o
                             int Skv, int causal, float scale, uint8_t* base, cudaStream_t stream, int dev) {
   const int kv_cap = Skv;
   using SL = SkLayout<HD>;
-  auto kern = fa_prefill_sk_kernel<HD, BF16>;
   SkParams sp;
   std::memset(&sp, 0, sizeof(sp));
   Params& prm = sp.p;
@@ -1992,14 +2034,8 @@ static int launch_sk_static(const void* q, const void* k, const void* v, void* o
   std::memcpy(sp.ph, sc.ph, sizeof(short) * sc.G);
   sp.ws_ml = reinterpret_cast<float*>(base);
   sp.ws_o = reinterpret_cast<float4*>(base + STATIC_O_OFF);
-  const int slot = (HD == 128 ? 2 : 0) + (BF16 ? 1 : 0);
-  if (g_sk_attr_set[dev][slot].load() == 0) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SL::REQUEST) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return FA_ERR_SMEM;
-    }
-    g_sk_attr_set[dev][slot].store(1);
-  }
+  auto kern = sc.one_seg ? fa_prefill_sk_kernel<HD, BF16, true> : fa_prefill_sk_kernel<HD, BF16, false>;
+  if (!sk_attr(kern, dev, (HD == 128 ? 2 : 0) + (BF16 ? 1 : 0) + (sc.one_seg ? 4 : 0), SL::REQUEST)) return FA_ERR_SMEM;
   EncodeTiledFn enc = encoder();
   if (!enc) return FA_ERR_LAUNCH;
   CUtensorMap mq, mk, mv, mo;

@@ -126,10 +126,13 @@ int fa_prefill_bf16(const void* q, const void* k, const void* v, void* o,
 
 /*
  * fa_prefill_ws / fa_prefill_ws_bf16 -- the same operation computed by a
- * persistent, load-balanced ("stream-K" / split-KV) kernel: one CTA per SM,
- * each taking an equal share of all (query-tile pair, KV tile) steps, so short
- * prompts, single heads and causal rows of very different lengths keep every
- * SM busy.  A query-tile pair whose KV steps are split between CTAs is merged
+ * load-balanced split-KV kernel: at most one CTA per SM.  With no more
+ * query-tile pairs than SMs, each pair is cut into near-equal pieces of its
+ * KV steps and every CTA computes one piece; with more pairs, the CTAs are
+ * persistent and each takes an equal contiguous share of all (query-tile
+ * pair, KV tile) steps ("stream-K").  Either way short prompts, single heads
+ * and causal rows of very different lengths keep every SM busy.  A
+ * query-tile pair whose KV steps are split between CTAs is merged
  * by a second, short kernel enqueued behind the first (programmatic dependent
  * launch), over the whole GPU and in a fixed order (results are
  * deterministic, run to run); this is the
