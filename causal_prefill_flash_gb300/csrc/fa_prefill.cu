@@ -115,8 +115,8 @@ struct Layout {
   static constexpr uint32_t OFF_Q = 0;               // Q_A, Q_B
   static constexpr uint32_t OFF_RING = 2 * Q_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_RING + NSLOT * SLOT_BYTES;
-  // q_full (Q and K_0), pair[NPB <= NSLOT] (V_j, K_j+1), empty[NSLOT], s_full[2], p_full[2], o_final,
-  // drain, o_staged[2]
+  // q_full (Q and K_0), pair[NPB <= NSLOT] (V_j, K_j+1), empty[NSLOT] (hd 128: pair-empty, NPE of them),
+  // s_full[2], p_full[2], o_final, drain, o_staged[2]
   static constexpr uint32_t NUM_BARS = 1 + 2 * NSLOT + 2 + 2 + 2 + 2;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
   static constexpr uint32_t BYTES = OFF_MISC + 16;
@@ -299,6 +299,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // pair j: its V's ring slot is freed only by P V(j) or a later MMA.
   constexpr int NPB = (NSLOT + 1) / 2;
   static_assert(2 * NPB >= NSLOT && NPB <= NSLOT, "pair barriers");
+  // At hd 128, K_j and V_j free their ring slots together, on one commit
+  // after P V_B(j) (one commit per step fewer for the MMA thread; measured
+  // +0.5 to +0.8 %, and -2 % at hd 64, whose ring keeps per-slot frees).  The
+  // producer waits on the pair-empty barrier of the slot's previous occupant;
+  // with 2 NPE > NSLOT, pair j+NPE cannot be freed before the producer's waits
+  // on pair j (its V is loaded only after them).
+  constexpr bool PAIR_EMPTY = HD == 128;
+  constexpr int NPE = NSLOT / 2 + 1;
+  static_assert(2 * NPE > NSLOT && NPE <= NSLOT, "pair-empty barriers");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -381,7 +390,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       for (int i = 0; i < 2 * n; ++i) {
         const int s = i % NSLOT;
-        if (i >= NSLOT) ok = wait_bar(bEmpty(s), ((i / NSLOT) & 1) ^ 1u, abort_flag, p.watchdog_ns, WD_PRODUCER_EMPTY);
+        if (i >= NSLOT) {
+          if constexpr (PAIR_EMPTY) {  // the previous occupant, load i - NSLOT, belongs to pair e
+            const int e = (i - NSLOT) >> 1;
+            ok = wait_bar(bEmpty(e % NPE), (e / NPE) & 1, abort_flag, p.watchdog_ns, WD_PRODUCER_EMPTY);
+          } else {
+            ok = wait_bar(bEmpty(s), ((i / NSLOT) & 1) ^ 1u, abort_flag, p.watchdog_ns, WD_PRODUCER_EMPTY);
+          }
+        }
         if (!ok) break;
         const int key0 = (i >> 1) * BN;
         int row = key0, bat = w.b;
@@ -457,7 +473,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::tc_fence_after();
         if (nA > 0) issue_s(0, 0);
         if (nB > 0) issue_s(1, 0);
-        ptx::mma_commit(bEmpty(0));
+        if constexpr (!PAIR_EMPTY) ptx::mma_commit(bEmpty(0));
       }
       for (int j = 0; ok && j < n; ++j) {
         const int iv = 2 * j + 1, sv = iv % NSLOT;  // V_j
@@ -474,11 +490,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::tc_fence_after();
             issue_pv(x, sv, j > 0);
           }
-          if (x == 1) ptx::mma_commit(bEmpty(sv));  // V_j no longer needed once PV_B(j) is done
+          if (x == 1) {
+            if constexpr (PAIR_EMPTY)
+              ptx::mma_commit(bEmpty(j % NPE));  // K_j (its S MMAs came earlier) and V_j, once P V_B(j) is done
+            else
+              ptx::mma_commit(bEmpty(sv));  // V_j no longer needed once PV_B(j) is done
+          }
           if (more && j + 1 < nX) issue_s(x, sk);
         }
         if (!ok) break;
-        if (more) ptx::mma_commit(bEmpty(sk));
+        if constexpr (!PAIR_EMPTY) {
+          if (more) ptx::mma_commit(bEmpty(sk));
+        }
       }
       if (ok) ptx::mma_commit(bOfinal);
       // every MMA issued has finished before TMEM is freed (the softmax may
