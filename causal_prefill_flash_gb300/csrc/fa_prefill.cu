@@ -118,7 +118,8 @@ struct Layout {
   // q_full (Q and K_0), pair[NPB <= NSLOT] (V_j, K_j+1), empty[NSLOT] (hd 128: pair-empty, NPE of them),
   // s_full[2], p_full[2], o_final, drain, o_staged[2]
   static constexpr uint32_t NUM_BARS = 1 + 2 * NSLOT + 2 + 2 + 2 + 2;
-  static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
+  // [0] TMEM base, [1] abort flag, [2], [3] barrier and phase of tile A's early o_final (0: none)
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr uint32_t BYTES = OFF_MISC + 16;
   static constexpr uint32_t REQUEST = BYTES + 1024;  // slack to align the dynamic base
   // TMEM columns: S_A | S_B | O_A | O_B (P_X overwrites the first BN/2 columns of S_X)
@@ -348,6 +349,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::mbar_init(bOstaged(0), 4);  // one arrival per softmax warp of the tile
     ptx::mbar_init(bOstaged(1), 4);
     misc[1] = 0u;
+    // tile A's early o_final (row pairs): the slot-free barrier of step nA-1
+    uint32_t early_bar = 0u, early_par = 0u;
+    if (!p.pair_heads && nA > 0 && nA < n) {
+      const int e = nA - 1;
+      if constexpr (PAIR_EMPTY) {
+        early_bar = bEmpty(e % NPE);
+        early_par = (e / NPE) & 1;
+      } else {
+        early_bar = bEmpty((2 * e + 1) % NSLOT);
+        early_par = ((2 * e + 1) / NSLOT) & 1;
+      }
+    }
+    misc[2] = early_bar;
+    misc[3] = early_par;
     ptx::mbar_fence_init();
   }
   if (warp == MMA_WARP) {
@@ -614,12 +629,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::mbar_arrive(bPfull(x));
     }
     // ------------------------------------------------------------ epilogue
-    // Once o_final has completed, every K/V load the CTA issued has been
-    // consumed, so the ring is idle: slot x stages O_X.  (Waited whenever the
-    // CTA streams any KV tile, even if this tile has none: the ring is busy
-    // until then.)
+    // Once o_final has completed, no MMA reads the ring any more.  Row pairs
+    // (tile B one KV tile longer than tile A): tile A's O is final once the
+    // ring slots of step nA-1 are freed, a commit the MMA thread issues after
+    // P V_B(nA-1) anyway, so tile A's epilogue runs under tile B's last step
+    // (measured +2 % at 2048 and 2659 tokens, +13 % on one 256-token head;
+    // no instruction added to the MMA thread).  No later commit reaches that
+    // barrier: its next one would be step nA-1+NPE (or, per slot, load
+    // 2 nA - 1 + NSLOT), past the last.  (Waited whenever the CTA streams any
+    // KV tile, even if this tile has none.)
+    // (The barrier and phase come from shared memory, set up by thread 0, so
+    // the softmax keeps no extra register live through its loop.)
     if (ok && n > 0) {
-      ok = warp_wait_bar(bOfinal, 0, abort_flag, p.watchdog_ns, WD_SOFTMAX_O_DONE);
+      const bool early = x == 0 && misc[2] != 0u;
+      ok = warp_wait_bar(early ? misc[2] : bOfinal, early ? misc[3] : 0u, abort_flag, p.watchdog_ns,
+                         WD_SOFTMAX_O_DONE);
       if (ok) ptx::tc_fence_after();
     }
     if (ok && hasx) {
@@ -628,7 +652,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // tile) and sent out by TMA tensor stores, one per 64-column block: the
       // global writes are whole lines, and rows past Sq are clipped by the map.
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-      const uint32_t stage = sRing + x * L::SLOT_BYTES + r * 128;
+      // Stage slots: tile A in the slot of load 2n-4 (K_n-2), tile B in that
+      // of load 2n-3 (V_n-2).  When tile A's O is final, only loads from
+      // 2n-3 on can still be read (P V_B(n-2), S_B(n-1), P V_B(n-1)), and
+      // no load is issued after 2n-1, so both slots stay free.
+      const int stage_slot = (2 * n + 2 * NSLOT - 4 + x) % NSLOT;
+      const uint32_t stage = sRing + stage_slot * L::SLOT_BYTES + r * 128;
       uint32_t orr[HD];  // the whole row: all loads in flight before one wait
       if (nX > 0) {
 #pragma unroll
@@ -656,7 +685,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (ok && lane == 0) {
 #pragma unroll
           for (int c = 0; c < (int)L::KCH; ++c)
-            ptx::tma_store_4d(&tmO, sRing + x * L::SLOT_BYTES + c * (BM * 128), c * 64, hqx, q0, w.b);
+            ptx::tma_store_4d(&tmO, sRing + stage_slot * L::SLOT_BYTES + c * (BM * 128), c * 64, hqx, q0, w.b);
           ptx::bulk_commit();
           ptx::bulk_wait_read0();  // the slot must stay valid until the TMA unit has read it
         }
