@@ -349,9 +349,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::mbar_init(bOstaged(0), 4);  // one arrival per softmax warp of the tile
     ptx::mbar_init(bOstaged(1), 4);
     misc[1] = 0u;
-    // tile A's early o_final (row pairs): the slot-free barrier of step nA-1
+    // tile A's early o_final (row pairs, hd 128): the slot-free barrier of step nA-1
     uint32_t early_bar = 0u, early_par = 0u;
-    if (!p.pair_heads && nA > 0 && nA < n) {
+    if (HD == 128 && !p.pair_heads && nA > 0 && nA < n) {
       const int e = nA - 1;
       if constexpr (PAIR_EMPTY) {
         early_bar = bEmpty(e % NPE);
@@ -641,7 +641,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // (The barrier and phase come from shared memory, set up by thread 0, so
     // the softmax keeps no extra register live through its loop.)
     if (ok && n > 0) {
-      const bool early = x == 0 && misc[2] != 0u;
+      const bool early = HD == 128 && x == 0 && misc[2] != 0u;  // hd 64: -2.5 % from the code alone
       ok = warp_wait_bar(early ? misc[2] : bOfinal, early ? misc[3] : 0u, abort_flag, p.watchdog_ns,
                          WD_SOFTMAX_O_DONE);
       if (ok) ptx::tc_fence_after();
