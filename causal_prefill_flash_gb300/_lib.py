@@ -46,6 +46,7 @@ _SIG = {
     "fa_debug_status": (_I, []),
     "fa_debug_status_clear": (_I, []),
     "fa_debug_set_watchdog_ns": (_I, [ctypes.c_ulonglong]),
+    "fa_debug_schedule": (_I, [_I] * 7 + [_P, _P, _P, _I, _P]),
 }
 
 
@@ -92,6 +93,26 @@ def debug_set_watchdog_ns(ns: int) -> None:
     """Testing hook: the limit (ns) each pipeline wait of later launches may
     take before its CTA gives up and reports it (0 restores the 2 s default)."""
     load().fa_debug_set_watchdog_ns(int(ns))
+
+
+def debug_schedule(B, Hq, Hkv, Sq, Skv, causal=True, sms=152):
+    """The split-KV work split for a shape (host-only): a dict with the per-CTA
+    start (pair, KV step) lists including the end entry, each pair's KV steps,
+    the CTA count, whether every CTA runs one segment, the split pairs and the
+    piece slots used."""
+    n_max = 4096
+    cp = (ctypes.c_int * 257)()
+    cs = (ctypes.c_int * 257)()
+    ps = (ctypes.c_int * n_max)()
+    out = (ctypes.c_int * 4)()
+    nu = int(load().fa_debug_schedule(int(B), int(Hq), int(Hkv), int(Sq), int(Skv), int(bool(causal)), int(sms),
+                                      ctypes.addressof(cp), ctypes.addressof(cs), ctypes.addressof(ps), n_max,
+                                      ctypes.addressof(out)))
+    if nu < 0:
+        raise FaError(-nu, "fa_debug_schedule")
+    G = out[0]
+    return {"pairs": nu, "ctas": G, "one_segment": bool(out[1]), "split_pairs": out[2], "slots": out[3],
+            "cta_pair": list(cp[: G + 1]), "cta_step": list(cs[: G + 1]), "pair_steps": list(ps[:nu])}
 
 
 def _ptr(x) -> int:

@@ -2217,6 +2217,39 @@ extern "C" const char* fa_status_string(int status) {
   }
 }
 
+extern "C" int fa_debug_schedule(int B, int Hq, int Hkv, int Sq, int Skv, int causal, int sms, int* cta_pair,
+                                 int* cta_step, int* pair_steps, int max_pairs, int* out) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Sq < 1 || Skv < 1 || sms < 1 || !cta_pair || !cta_step || !out)
+    return -FA_ERR_INVALID_ARG;
+  fa::Params prm;
+  std::memset(&prm, 0, sizeof(prm));
+  prm.B = B;
+  prm.Hq = Hq;
+  prm.Hkv = Hkv;
+  prm.Sq = Sq;
+  prm.Skv = Skv;
+  prm.G = Hq / Hkv;
+  prm.n_qtiles = (Sq + fa::BM - 1) / fa::BM;
+  prm.pair_heads = (prm.G % 2 == 0) ? 1 : 0;
+  prm.causal = causal ? 1 : 0;
+  const long long nu = fa::unit_count_of(prm);
+  if (nu > 0x7FFFFFFF) return -FA_ERR_UNSUPPORTED;
+  if (pair_steps && nu > max_pairs) return -FA_ERR_UNSUPPORTED;
+  fa::SkSchedule sc;
+  fa::make_schedule(prm, sms, &sc);
+  for (int c = 0; c <= sc.G; ++c) {
+    cta_pair[c] = sc.su[c];
+    cta_step[c] = sc.sj[c];
+  }
+  if (pair_steps)
+    for (long long u = 0; u < nu; ++u) pair_steps[u] = fa::unit_geo(prm, static_cast<int>(u)).n;
+  out[0] = sc.G;
+  out[1] = sc.one_seg;
+  out[2] = sc.n_split;
+  out[3] = sc.slots;
+  return static_cast<int>(nu);
+}
+
 extern "C" unsigned int fa_smem_bytes(int hd) {
   if (fa::kernel_hd(hd) == 256) return fa::Layout256::REQUEST;
   if (fa::kernel_hd(hd) == 128) return fa::Layout<128>::REQUEST;

@@ -78,6 +78,7 @@
  *   fa_prefill_ws_static             split-KV with library-owned scratch
  *   fa_status_string, fa_smem_bytes, fa_debug_status(_clear)  diagnostics
  *   fa_debug_set_watchdog_ns         testing hook: the kernels' wait limit
+ *   fa_debug_schedule                the split-KV work split for a shape
  */
 #ifndef FA_PREFILL_H
 #define FA_PREFILL_H
@@ -390,6 +391,28 @@ int fa_debug_status_clear(void);
  * process-wide.  Returns FA_OK.
  */
 int fa_debug_set_watchdog_ns(unsigned long long ns);
+
+/*
+ * fa_debug_schedule -- the work split fa_prefill_ws launches for a shape on
+ * a GPU of `sms` SMs (host-only, no device call; for tests and tools).  The
+ * query-tile pairs ("pairs") are numbered like the one-shot grid, longest
+ * first.  CTA c starts at pair cta_pair[c], KV step cta_step[c], and ends
+ * where CTA c+1 starts; entry [ctas] is the end (pair count, step 0).
+ *   cta_pair, cta_step   host arrays of at least 257 ints (written)
+ *   pair_steps           host array of at least max_pairs ints receiving
+ *                        each pair's KV steps, or NULL
+ *   out                  host array of 4 ints (written): CTAs, 1 if every
+ *                        CTA runs a single segment (no more pairs than CTAs:
+ *                        each pair cut into near-equal pieces), pairs split
+ *                        between CTAs (merged by the second kernel), piece
+ *                        slots used in the workspace
+ * Returns the number of pairs (>= 0), -FA_ERR_INVALID_ARG for a bad shape,
+ * sms < 1 or a NULL array, -FA_ERR_UNSUPPORTED when pair_steps is given and
+ * there are more than max_pairs pairs.
+ */
+int fa_debug_schedule(int B, int Hq, int Hkv, int Sq, int Skv, int causal, int sms,
+                      int* cta_pair, int* cta_step, int* pair_steps, int max_pairs,
+                      int* out);
 
 #ifdef __cplusplus
 }
