@@ -822,6 +822,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   using L = Layout<HD>;
   using SL = SkLayout<HD>;
   constexpr int NSLOT = SL::NSLOT;
+  // One-segment CTAs take the one-shot kernel's K/V protocol: K_jb arrives
+  // with Q, then V_t and K_t+1 on pair barrier t % NPB (full[0 .. NPB)), one
+  // wait per step for the MMA thread (same reuse rule: 2 NPB >= NSLOT).
+  constexpr int NPB = (NSLOT + 1) / 2;
+  static_assert(2 * NPB >= NSLOT && NPB <= NSLOT, "pair barriers");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -854,7 +859,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::mbar_init(bQfull, 1);
     ptx::mbar_init(bQempty, 1);
     for (int s = 0; s < NSLOT; ++s) {
-      ptx::mbar_init(bFull(s), 1);
+      ptx::mbar_init(bFull(s), ONE_SEG && s < NPB ? 2 : 1);  // pair barriers: one arrival per load
       ptx::mbar_init(bEmpty(s), 1);
     }
     for (int x = 0; x < 2; ++x) {
@@ -900,7 +905,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (je <= jb) continue;  // nothing to stream (the softmax writes zeros)
         if (nq > 0) ok = wait_bar(bQempty, (nq - 1) & 1, abort_flag, p.watchdog_ns, WD_PRODUCER_EMPTY);
         if (!ok) break;
-        ptx::mbar_arrive_expect_tx(bQfull, L::Q_BYTES * (w.has1 ? 2u : 1u));
+        ptx::mbar_arrive_expect_tx(bQfull, L::Q_BYTES * (w.has1 ? 2u : 1u) + (ONE_SEG ? L::SLOT_BYTES : 0u));
 #pragma unroll
         for (int c = 0; c < (int)L::KCH; ++c)
           ptx::tma_load_4d(sQ + c * (BM * 128), &tmQ, bQfull, c * 64, w.hq0, w.q00, w.b);
@@ -942,18 +947,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bat = blk;
             tail = pg == p.last_page;
           }
-          ptx::mbar_arrive_expect_tx(bFull(s), L::SLOT_BYTES);
+          uint32_t fb = bFull(s);
+          if constexpr (ONE_SEG) {  // g counts this segment's loads: K_jb, then pairs (V, K)
+            const int pj = (g - 1) >> 1;
+            fb = g == 0 ? bQfull : bFull(pj % NPB);
+            if ((g & 1) && pj >= NPB) {  // pair pj reuses pair pj-NPB's barrier
+              ok = wait_bar(fb, ((pj - NPB) / NPB) & 1, abort_flag, p.watchdog_ns, WD_PRODUCER_EMPTY);
+              if (!ok) break;
+            }
+            if (g > 0) ptx::mbar_arrive_expect_tx(fb, L::SLOT_BYTES);
+          } else {
+            ptx::mbar_arrive_expect_tx(fb, L::SLOT_BYTES);
+          }
           const CUtensorMap* m = (i & 1) ? (tail ? &tmVt : &tmV) : (tail ? &tmKt : &tmK);
 #pragma unroll
           for (int c = 0; c < (int)L::KCH; ++c)
-            ptx::tma_load_4d(sRing + s * L::SLOT_BYTES + c * (BN * 128), m, bFull(s), c * 64, w.hk, row, bat);
+            ptx::tma_load_4d(sRing + s * L::SLOT_BYTES + c * (BN * 128), m, fb, c * 64, w.hk, row, bat);
         }
       }
+      // a pair whose K was not issued (the last V, or a CTA that gave up)
+      if (ONE_SEG && g >= 2 && (g & 1) == 0) ptx::mbar_arrive(bFull(((g - 2) >> 1) % NPB));
       // every copy issued has landed before the CTA exits (as in the one-shot kernel)
       if (nq > 0) drain_wait(bQfull, (nq - 1) & 1, DRAIN_NS);
-      for (int s = 0; s < NSLOT && s < g; ++s) {
-        const int last = s + NSLOT * ((g - 1 - s) / NSLOT);
-        drain_wait(bFull(s), (last / NSLOT) & 1, DRAIN_NS);
+      if constexpr (ONE_SEG) {
+        const int npairs = g / 2;  // pairs armed
+        for (int b = 0; b < NPB && b < npairs; ++b) {
+          const int last = b + NPB * ((npairs - 1 - b) / NPB);
+          drain_wait(bFull(b), (last / NPB) & 1, DRAIN_NS);
+        }
+      } else {
+        for (int s = 0; s < NSLOT && s < g; ++s) {
+          const int last = s + NSLOT * ((g - 1 - s) / NSLOT);
+          drain_wait(bFull(s), (last / NSLOT) & 1, DRAIN_NS);
+        }
       }
     } else if (warp == MMA_WARP && lane == 0) {
       // ------------------------------------------------------- MMA issuer
@@ -995,8 +1021,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ok = wait_bar(bQfull, nq & 1, abort_flag, p.watchdog_ns, WD_MMA_Q);
         if (!ok) break;
         const int gK = g;  // ring index of K_jb; V_(jb+t) = gK + 2t + 1, K_(jb+t) = gK + 2t
-        ok = wait_bar(bFull(gK % NSLOT), (gK / NSLOT) & 1, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);
-        if (!ok) break;
+        if constexpr (!ONE_SEG) {  // one segment: K_jb came with Q
+          ok = wait_bar(bFull(gK % NSLOT), (gK / NSLOT) & 1, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);
+          if (!ok) break;
+        }
         ptx::tc_fence_after();
         if (nAs > 0) issue_s(0, gK % NSLOT);
         if (nBs > 0) issue_s(1, gK % NSLOT);
@@ -1006,11 +1034,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int iv = gK + 2 * t + 1, sv = iv % NSLOT;
           const int ik = gK + 2 * t + 2, sk = ik % NSLOT;
           const bool more = t + 1 < nseg;
-          ok = wait_bar(bFull(sv), (iv / NSLOT) & 1, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);
-          if (!ok) break;
-          if (more) {
-            ok = wait_bar(bFull(sk), (ik / NSLOT) & 1, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);
+          if constexpr (ONE_SEG) {
+            ok = wait_bar(bFull(t % NPB), (t / NPB) & 1, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);  // V_t, K_t+1
             if (!ok) break;
+          } else {
+            ok = wait_bar(bFull(sv), (iv / NSLOT) & 1, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);
+            if (!ok) break;
+            if (more) {
+              ok = wait_bar(bFull(sk), (ik / NSLOT) & 1, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);
+              if (!ok) break;
+            }
           }
 #pragma unroll
           for (int x = 0; x < 2; ++x) {
