@@ -48,8 +48,8 @@
 // global memory is touched only after griddepcontrol.wait.
 //
 // The same translation unit holds the other kernels of the library, which
-// share these helpers: the persistent split-KV kernel (fa_prefill_sk_kernel,
-// below), the hd = 256 kernel (fa_prefill256.cuh) and the K/V-cache append
+// share these helpers: the split-KV kernel (fa_prefill_sk_kernel, below),
+// the hd = 256 kernel (fa_prefill256.cuh) and the K/V-cache append
 // (kv_append.cuh).
 
 #include <cuda.h>
@@ -714,18 +714,21 @@ namespace fa {
 // The one-shot kernel above gives every CTA whole query-tile pairs, so a grid
 // with few or uneven pairs (short prompts, one head, causal rows of very
 // different lengths) leaves SMs idle and pays the pipeline fill and drain once
-// per CTA.  This kernel runs one persistent CTA per SM and cuts the whole
-// iteration space -- (query-tile pair, KV tile) steps, pairs longest first --
-// into equal contiguous ranges, one per CTA.  A pair whose steps straddle a
-// range boundary is computed in pieces: every piece leaves its unnormalised
-// O, running max m and sum l in a workspace slot the host assigned, and a
-// second, short kernel (fa_sk_merge_kernel, chained by programmatic
-// dependent launch) combines each split pair's pieces over the whole GPU in a
-// fixed order, so results are deterministic.  No CTA waits on another.
+// per CTA.  This kernel runs at most one CTA per SM over the whole iteration
+// space -- (query-tile pair, KV tile) steps, pairs longest first.  With no
+// more pairs than CTAs each pair is cut into near-equal pieces and every CTA
+// computes one (the ONE_SEG instantiation: a single step loop, as in the
+// one-shot kernel); otherwise the CTAs are persistent and each takes an equal
+// contiguous range of steps.  A pair whose steps straddle a range boundary
+// is computed in pieces: every piece leaves its unnormalised O, running max m
+// and sum l in a workspace slot the host assigned, and a second, short kernel
+// (fa_sk_merge_kernel, chained by programmatic dependent launch) combines
+// each split pair's pieces over the whole GPU in a fixed order, so results
+// are deterministic.  No CTA waits on another.
 
 constexpr int SK_MAX_CTAS = 256;
-// The persistent loop keeps more state in the control warps than the
-// one-shot kernel: its own register split (same launch allocation).
+// The segment loop keeps more state in the control warps than the one-shot
+// kernel: its own register split (same launch allocation).
 constexpr uint32_t SK_REGS_SOFTMAX = 200;
 constexpr uint32_t SK_REGS_CONTROL = 88;
 static_assert(128 * SK_REGS_CONTROL + 256 * SK_REGS_SOFTMAX <= NUM_THREADS * LAUNCH_REGS,
@@ -748,12 +751,13 @@ struct SkParams {
 template <int HD>
 struct SkLayout {
   using L = Layout<HD>;
-  // The persistent CTA keeps loading the next segment's K/V while it writes
-  // the previous segment's O, so O cannot be staged in the ring: each softmax
-  // thread writes its row straight from registers, and the ring keeps the
-  // one-shot kernel's depth.
+  // A persistent CTA keeps loading the next segment's K/V while it writes the
+  // previous segment's O, so O cannot be staged in the ring: each softmax
+  // thread writes its row straight from registers (or its piece to the
+  // workspace), and the ring keeps the one-shot kernel's depth.
   static constexpr int NSLOT = HD == 128 ? 5 : 8;
-  // q_full, q_empty, full[NSLOT], empty[NSLOT], s_full[2], p_full[2], o_final[2], drain
+  // q_full, q_empty, full[NSLOT] (ONE_SEG: pair barriers, the first NPB), empty[NSLOT], s_full[2],
+  // p_full[2], o_final[2], drain
   static constexpr uint32_t NUM_BARS = 2 + 2 * NSLOT + 2 + 2 + 2 + 1;
   static constexpr uint32_t OFF_BAR = L::OFF_RING + NSLOT * L::SLOT_BYTES;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
