@@ -129,3 +129,27 @@ def test_schedule_rejects_bad_shapes(fa):
             fa.debug_schedule(*bad, sms=SMS)
     with pytest.raises(fa.FaError):
         fa.debug_schedule(1, 8, 2, 128, 128, True, sms=0)
+
+
+def test_static_scratch_bound_holds_for_every_schedule(fa):
+    """fa_prefill_ws_static's documented bound: pieces <= 2 * CTAs - 1, so a
+    152-SM GPU needs at most 1048576 + 303 * 1024 * 128 = 40763392 bytes of the
+    40 MiB static scratch at hd 128.  A seeded sweep of shapes (GQA and MHA,
+    causal and not, chunked and square, tiny to many pairs)."""
+    import random
+    rng = random.Random(7)
+    worst = 0
+    for _ in range(300):
+        G = rng.choice([1, 2, 4, 8])
+        Hkv = rng.choice([1, 2, 4, 8])
+        Hq = G * Hkv
+        B = rng.choice([1, 1, 2, 4])
+        Sq = rng.choice([1, 77, 128, 300, 512, 1000, 2048, 2659])
+        Skv = Sq + rng.choice([0, 0, 128, 1000, 7680, 32640])
+        causal = rng.random() < 0.8
+        sc = fa.debug_schedule(B, Hq, Hkv, Sq, Skv, causal, sms=SMS)
+        assert sc["slots"] <= 2 * sc["ctas"] - 1
+        need = 1048576 + sc["slots"] * 1024 * 128
+        worst = max(worst, need)
+        assert need <= 40 * 1024 * 1024
+    assert worst <= 40763392
