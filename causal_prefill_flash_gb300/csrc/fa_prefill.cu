@@ -2127,12 +2127,15 @@ static int launch_sk_static(const void* q, const void* k, const void* v, void* o
   if (!sk_attr(kern, dev, (HD == 128 ? 2 : 0) + (BF16 ? 1 : 0) + (sc.one_seg ? 4 : 0), SL::REQUEST)) return FA_ERR_SMEM;
   EncodeTiledFn enc = encoder();
   if (!enc) return FA_ERR_LAUNCH;
-  CUtensorMap mq, mk, mv, mo;
-  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, hd, Sq) || !encode_bshd(&mk, enc, k, BF16, B, Skv, Hkv, HD, kv_cap) ||
-      !encode_bshd(&mv, enc, v, BF16, B, Skv, Hkv, HD, kv_cap) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, hd, Sq))
+  // the maps describe the caller's head width hd (<= HD): TMA zero-fills the
+  // missing columns and never reads past the tensors
+  CUtensorMap mq, mk, mv, mo, mkt, mvt;
+  Params pkv;
+  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, hd, Sq) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, hd, Sq) ||
+      !encode_kv(&mk, &mv, &mkt, &mvt, enc, k, v, BF16, B, Skv, kv_cap, Hkv, hd, nullptr, &pkv))
     return FA_ERR_LAUNCH;
-  if (launch_pdl(kern, dim3(static_cast<unsigned>(sc.G)), dim3(NUM_THREADS), SL::REQUEST, stream, mq, mk, mv, mo, mk,
-                 mv, sp) != cudaSuccess) {
+  if (launch_pdl(kern, dim3(static_cast<unsigned>(sc.G)), dim3(NUM_THREADS), SL::REQUEST, stream, mq, mk, mv, mo, mkt,
+                 mvt, sp) != cudaSuccess) {
     (void)cudaGetLastError();
     return FA_ERR_LAUNCH;
   }
