@@ -88,14 +88,21 @@ PLANTED_MISTAKES = {
     "none": 0, "no_scale": 1, "top_left": 2, "mask_off_by_one": 3, "gqa_modulo": 4,
     "no_normalise": 5, "v_reversed": 6, "no_max_subtract": 7, "exp2": 8, "masked_row_nan": 9,
     "round_truncate": 10, "round_ties_away": 11, "append_at_t": 12, "lse_log2": 13,
+    "gather_swapped": 14, "gather_no_table": 15,
 }
+# mistakes planted in this file's own arithmetic (the paged gather) rather than in the C library
+_PY_PLANTS = ("gather_swapped", "gather_no_table")
+_py_plant = "none"
 
 
 def plant_mistake(kind: str) -> None:
     """Switch the oracle to one planted mistake (``"none"`` restores it). Tests only."""
-    rc = _load().oracle_plant_mistake(PLANTED_MISTAKES[kind])
+    global _py_plant
+    code = PLANTED_MISTAKES[kind]
+    rc = _load().oracle_plant_mistake(0 if kind in _PY_PLANTS else code)
     if rc != 0:
         raise ValueError(kind)
+    _py_plant = kind if kind in _PY_PLANTS else "none"
 
 
 def _f64(x) -> np.ndarray:
@@ -214,7 +221,12 @@ def gather_pages(pool, block_table, kv_len: int, page_size: int):
     pool = np.asarray(pool.detach().cpu().double().numpy() if hasattr(pool, "detach") else pool, dtype=np.float64)
     table = np.asarray(block_table.cpu().numpy() if hasattr(block_table, "cpu") else block_table, dtype=np.int64)
     j = np.arange(kv_len)
-    return np.ascontiguousarray(pool[table[:, j // page_size], j % page_size])
+    page, row = j // page_size, j % page_size
+    if _py_plant == "gather_swapped":  # planted mistake: page and row index exchanged
+        page, row = row, page
+    if _py_plant == "gather_no_table":  # planted mistake: the page number used as the pool block
+        return np.ascontiguousarray(np.broadcast_to(pool[page, row], (table.shape[0],) + pool[page, row].shape))
+    return np.ascontiguousarray(pool[table[:, page], row])
 
 
 def lse_rows(q, k, rows, causal: bool = True, scale: float | None = None) -> np.ndarray:

@@ -451,18 +451,44 @@ def test_lse_by_brute_force_and_closed_forms():
     assert abs(got3[0, 0, 1] - scale * float(np.dot(q[0, 1, 0], k[0, 0, 0]))) < 1e-12
 
 
-def test_gather_pages_by_brute_force():
-    """The paged-cache gather against a loop over every key: key j of sequence
-    b is row j % page of block table[b][j // page]."""
-    rng = np.random.default_rng(3)
-    nb, page, Hkv, hd, B, kv_len = 9, 4, 2, 3, 2, 11
-    pool = rng.standard_normal((nb, page, Hkv, hd))
-    table = np.stack([rng.permutation(nb)[:3] for _ in range(B)])
-    got = oracle.gather_pages(pool, table, kv_len, page)
-    assert got.shape == (B, kv_len, Hkv, hd)
+def _scatter_to_pages(kc, table, page, nb, fill):
+    """The inverse of a paged gather, written as a cache manager fills pages:
+    walk each sequence's table entries in order and copy the next `page`
+    keys into that block, row by row.  Pool rows no key lands in keep `fill`."""
+    B, kv_len = kc.shape[:2]
+    pool = np.full((nb, page) + kc.shape[2:], fill)
     for b in range(B):
-        for j in range(kv_len):
-            assert np.array_equal(got[b, j], pool[table[b, j // page], j % page])
+        src = 0  # next key of sequence b to place
+        for entry in table[b]:
+            for r in range(page):
+                if src >= kv_len:
+                    break
+                pool[entry, r] = kc[b, src]
+                src += 1
+    return pool
+
+
+def test_gather_pages_inverts_a_page_scatter():
+    """Scatter contiguous keys into a shuffled pool (the page walk above, which
+    never forms j // page or j % page), then gather them back through the block
+    table: the result must be the original keys, bit for bit.  Pool rows no key
+    was written to hold NaN, so a gather that reads any of them fails.  The
+    sizes keep every swapped index in range, so a page/row mix-up gives wrong
+    values rather than an index error."""
+    rng = np.random.default_rng(3)
+    B, kv_len, Hkv, hd, page, max_pages, nb = 2, 14, 2, 3, 4, 5, 12
+    kc = rng.standard_normal((B, kv_len, Hkv, hd))
+    perm = rng.permutation(nb)
+    table = perm[: B * max_pages].reshape(B, max_pages)
+    pool = _scatter_to_pages(kc, table, page, nb, np.nan)
+    got = oracle.gather_pages(pool, table, kv_len, page)
+    assert got.shape == kc.shape
+    assert np.array_equal(got, kc)
+    # a table that maps both sequences to the same blocks reads the same keys for both
+    shared = np.stack([table[0], table[0]])
+    pool2 = _scatter_to_pages(kc[:1], shared[:1], page, nb, np.nan)
+    got2 = oracle.gather_pages(pool2, shared, kv_len, page)
+    assert np.array_equal(got2[0], kc[0]) and np.array_equal(got2[1], kc[0])
 
 
 # --------------------------------------------------------------------------
@@ -492,6 +518,7 @@ def _pin_battery():
         ("round_ties", test_round_ties_go_to_even),
         ("kv_append", test_kv_append_scatters_rounded_rows_to_positions),
         ("lse", test_lse_by_brute_force_and_closed_forms),
+        ("gather_pages", test_gather_pages_inverts_a_page_scatter),
     ]
 
 
