@@ -8,7 +8,10 @@ epilogue).  Inputs are seeded synthetic tensors shaped like the pages' 7B
 prefill workloads, resident in HBM before the timed region; the step rotates
 over enough input copies that the working set exceeds L2, so every step reads
 Q/K/V from HBM.  Time is device time from CUDA events on the launching stream,
-bracketed by a barrier and a synchronize, max over ranks.
+bracketed by a barrier and a synchronize, max over ranks; the timed steps run
+as back-to-back bursts with an event between bursts, and ms/step is the median
+burst (the spread over bursts is printed beside it).  The default workload is
+the 8192-token GQA prefill (bf16, hd 128), the largest of the workloads.
 
 Prints one JSON line.  Under torchrun each rank runs its own replica of the
 workload on its own GPU (attention over independent (batch, head) problems
@@ -33,7 +36,8 @@ sys.path.insert(0, ROOT)
 L2_BYTES = 129 * 1024 * 1024
 REFERENCE_SECONDS = 90.0  # the whole reference arm (warmup + steps), whatever K and W
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-DEFAULT_WORKLOAD = "prefill7b_s2048"
+DEFAULT_WORKLOAD = "gqa_s8192_bf16"
+BURSTS = 11  # the timed steps are split into this many bursts; ms/step is their median
 
 
 def parse_args(argv=None):
@@ -82,6 +86,18 @@ def job_throughput(flops_per_step_per_rank: int, world: int, ms_per_step: float)
     """Whole-job TFLOP/s: every rank runs its own replica of the workload (weak
     scaling), all ranks' flops over the slowest rank's step time."""
     return flops_per_step_per_rank * world / (ms_per_step * 1e-3) / 1e12
+
+
+def burst_spread(per_burst):
+    """Median, 10th and 90th percentile (nearest rank) and extremes of the
+    per-burst ms/step figures."""
+    xs = sorted(per_burst)
+    n = len(xs)
+
+    def pct(p):
+        return xs[min(n - 1, max(0, math.ceil(p / 100.0 * n) - 1))]
+    return {"bursts": n, "median_ms": statistics.median(xs), "p10_ms": pct(10), "p90_ms": pct(90),
+            "min_ms": xs[0], "max_ms": xs[-1]}
 
 
 def load_peaks():
@@ -383,53 +399,93 @@ def run_ours(args):
         torch.cuda.synchronize()
         barrier()
         torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(args.steps):
-            step(i)
-        e1.record(stream)
+        # the K timed steps in back-to-back bursts, one CUDA event between
+        # bursts (an event between two launches ends their overlap, so there
+        # is one per burst, not one per step)
+        nb = max(1, min(BURSTS, args.steps))
+        sizes = [args.steps // nb + (1 if b < args.steps % nb else 0) for b in range(nb)]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(nb + 1)]
+        ev[0].record(stream)
+        i = 0
+        for b in range(nb):
+            for _ in range(sizes[b]):
+                step(i)
+                i += 1
+            ev[b + 1].record(stream)
         torch.cuda.synchronize()
         clocks.mark(t_load0, time.time())
         barrier()
         torch.cuda.synchronize()
-    ms_total = max_over_ranks(e0.elapsed_time(e1), dev)
-    ms_step = ms_total / args.steps
+    per_burst = [ev[b].elapsed_time(ev[b + 1]) / sizes[b] for b in range(nb)]
+    ms_total = max_over_ranks(ev[0].elapsed_time(ev[nb]), dev)
+    ms_step = max_over_ranks(statistics.median(per_burst), dev)
+    spread = burst_spread(per_burst)
     flops = w.flops()
     value = job_throughput(flops, world, ms_step)
     watchdog = fa.debug_status()
 
-    # end to end through the public API: pinned host inputs -> device -> kernel -> host O
+    # end to end through the public API: pinned host inputs -> device -> kernel
+    # -> host O, every step.  Three streams and two device buffer sets: step
+    # i+1's host-to-device copies run under step i's kernel and step i-1's
+    # device-to-host copy (opposite copy directions use separate engines).
+    # Events order each buffer set's reuse: the copy-in of step i waits for
+    # the kernel of step i-2 (done reading that set), the kernel of step i for
+    # its own copy-in and for the copy-out of step i-2 (done reading its O).
     e2e = None
     if not args.no_e2e and not paged:  # the e2e leg times the contiguous public API only
         hq_, hk_, hv_ = q.pin_memory(), k.pin_memory(), v.pin_memory()
-        ho = torch.empty_like(q).pin_memory()
-        dq, dk, dv = torch.empty_like(q, device=dev), torch.empty_like(k, device=dev), torch.empty_like(v, device=dev)
-        do = torch.empty_like(q, device=dev)
+        hos = [torch.empty_like(q).pin_memory() for _ in range(2)]
+        sets = [(torch.empty_like(q, device=dev), torch.empty_like(k, device=dev), torch.empty_like(v, device=dev),
+                 torch.empty_like(q, device=dev)) for _ in range(2)]
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_used = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
 
-        def e2e_step():
-            dq.copy_(hq_, non_blocking=True)
-            dk.copy_(hk_, non_blocking=True)
-            dv.copy_(hv_, non_blocking=True)
-            fa.attention(dq, dk, dv, causal=w.causal, scale=w.scale, out=do, split=split)
-            ho.copy_(do, non_blocking=True)
+        def e2e_step(i):
+            bi = i % 2
+            dq, dk, dv, do = sets[bi]
+            if i >= 2:
+                s_in.wait_event(ev_used[bi])
+            with torch.cuda.stream(s_in):
+                dq.copy_(hq_, non_blocking=True)
+                dk.copy_(hk_, non_blocking=True)
+                dv.copy_(hv_, non_blocking=True)
+            ev_in[bi].record(s_in)
+            stream.wait_event(ev_in[bi])
+            if i >= 2:
+                stream.wait_event(ev_out[bi])
+            fa.attention(dq, dk, dv, causal=w.causal, scale=w.scale, out=do, split=split, stream=stream)
+            ev_used[bi].record(stream)
+            s_out.wait_event(ev_used[bi])
+            with torch.cuda.stream(s_out):
+                hos[bi].copy_(do, non_blocking=True)
+            ev_out[bi].record(s_out)
 
-        for _ in range(3):
-            e2e_step()
+        def drain():
+            stream.wait_event(ev_out[0])
+            stream.wait_event(ev_out[1])
+
+        for i in range(3):
+            e2e_step(i)
+        drain()
         torch.cuda.synchronize()
         barrier()
         a0 = torch.cuda.Event(enable_timing=True)
         a1 = torch.cuda.Event(enable_timing=True)
-        a0.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
+        a0.record(s_in)
+        for i in range(args.e2e_steps):
+            e2e_step(i)
+        drain()
         a1.record(stream)
         torch.cuda.synchronize()
         ms_e2e = max_over_ranks(a0.elapsed_time(a1) / args.e2e_steps, dev)
         e2e = {"value": job_throughput(flops, world, ms_e2e), "unit": "TFLOP/s",
                "ms_per_step": ms_e2e,
                "h2d_bytes_per_step": int((q.numel() + k.numel() + v.numel()) * q.element_size()),
-               "d2h_bytes_per_step": int(q.numel() * q.element_size())}
+               "d2h_bytes_per_step": int(q.numel() * q.element_size()),
+               "pipeline": "copy-in, kernel and copy-out of consecutive steps on three streams, "
+                           "two device buffer sets"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -447,6 +503,8 @@ def run_ours(args):
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic",
+        "spread": dict(spread, ms_total=ms_total, note="ms/step of each burst of the timed steps; "
+                       "value and ms_per_step use the median"),
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Skv": w.Skv,
                    "hd": w.hd, "causal": w.causal, "scale": w.scale,
                    "flops_per_call": flops, "flop_convention": "4*hd*visible (query,key) pairs",
@@ -465,7 +523,7 @@ def run_ours(args):
         "clocks": clocks.summary(),
         "e2e": e2e,
         "cpu_baseline": cpu,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if split else 1),  # split-KV: the stream-K kernel and the merge
         "watchdog_status": watchdog,
     }
     print(json.dumps(line), flush=True)
