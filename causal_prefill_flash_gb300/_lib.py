@@ -46,6 +46,7 @@ _SIG = {
     "fa_debug_status": (_I, []),
     "fa_debug_status_clear": (_I, []),
     "fa_debug_set_watchdog_ns": (_I, [ctypes.c_ulonglong]),
+    "fa_debug_force_path": (_I, [ctypes.c_int]),
     "fa_debug_schedule": (_I, [_I] * 7 + [_P, _P, _P, _I, _P]),
 }
 
@@ -93,6 +94,19 @@ def debug_set_watchdog_ns(ns: int) -> None:
     """Testing hook: the limit (ns) each pipeline wait of later launches may
     take before its CTA gives up and reports it (0 restores the 2 s default)."""
     load().fa_debug_set_watchdog_ns(int(ns))
+
+
+PATHS = {"auto": 0, "oneshot": 1, "persistent": 2}
+
+
+def debug_force_path(path: str) -> None:
+    """Testing hook: the kernel later calls run on -- "auto" (the library's
+    choice), "oneshot" (the one-shot kernel, also for calls with a workspace)
+    or "persistent" (the persistent kernel: over whole units without a
+    workspace, over every split-KV schedule with one)."""
+    st = int(load().fa_debug_force_path(PATHS[path]))
+    if st != FA_OK:
+        raise FaError(st, "fa_debug_force_path")
 
 
 def debug_schedule(B, Hq, Hkv, Sq, Skv, causal=True, sms=152):

@@ -263,6 +263,15 @@ __device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity,
   return __all_sync(0xffffffffu, ok);
 }
 
+// The MMA warp's wait: warp-uniform when the whole warp runs the issue loop,
+// else the single issuing thread's.
+template <bool kWarp>
+__device__ __forceinline__ bool mma_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                         unsigned long long limit_ns, uint32_t code) {
+  if constexpr (kWarp) return warp_wait_bar(bar, parity, abort_flag, limit_ns, code);
+  else return wait_bar(bar, parity, abort_flag, limit_ns, code);
+}
+
 // Drain wait used only on the abort path: bounded, ignores the abort flag.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
   const uint64_t t0 = ptx::globaltimer_ns();
@@ -459,7 +468,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == MMA_WARP) {
     // ----------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // hd 64: the whole warp runs the loop and the waits and one elected lane
+    // issues (its N = 64 P V MMAs make the issuing rate matter: measured +6 %
+    // on the chunked hd 64 prefill); hd 128: lane 0 alone (the converged form
+    // measured -5 to +2 % there)
+    constexpr bool CONV = HD == 64;
+    const bool leader = CONV ? ptx::elect_one() : true;
+    if (CONV || lane == 0) {
       constexpr uint32_t IDESC_S = ptx::idesc_f16(BF16, BM, BN, false, false);  // Q, K both K-major
       constexpr uint32_t IDESC_O = ptx::idesc_f16(BF16, BM, HD, false, true);   // P from TMEM, V MN-major
       constexpr uint32_t DHI = ptx::sdesc_sw128_hi(1024);  // Q, K (K-major) and V (MN-major): SBO 1024
@@ -470,9 +485,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t o = ((kk / 4) * (BM * 128) + (kk % 4) * 32) >> 4;
-          ptx::mma_f16_ss(d, ptx::sdesc_join(q + o, DHI), ptx::sdesc_join(k + o, DHI), IDESC_S, kk > 0 ? 1u : 0u);
+          if (leader) ptx::mma_f16_ss(d, ptx::sdesc_join(q + o, DHI), ptx::sdesc_join(k + o, DHI), IDESC_S, kk > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(bSfull(x));
+        if (leader) ptx::mma_commit(bSfull(x));
       };
       auto issue_pv = [&](int x, int slot, bool acc) {
         const uint32_t d = tmem + L::TM_O + x * HD;
@@ -480,32 +495,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t v = ptx::sdesc_sw128_lo(sRing + slot * L::SLOT_BYTES, BN * 128);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          ptx::mma_f16_ts(d, a + kk * 8, ptx::sdesc_join(v + kk * ((16 * 128) >> 4), DHI), IDESC_O,
+          if (leader) ptx::mma_f16_ts(d, a + kk * 8, ptx::sdesc_join(v + kk * ((16 * 128) >> 4), DHI), IDESC_O,
                           (acc || kk > 0) ? 1u : 0u);
       };
-      bool ok = wait_bar(bQ, 0, abort_flag, p.watchdog_ns, WD_MMA_Q);  // Q and K_0
+      bool ok = mma_wait<CONV>(bQ, 0, abort_flag, p.watchdog_ns, WD_MMA_Q);  // Q and K_0
       if (ok && n > 0) {
         ptx::tc_fence_after();
         if (nA > 0) issue_s(0, 0);
         if (nB > 0) issue_s(1, 0);
-        if constexpr (!PAIR_EMPTY) ptx::mma_commit(bEmpty(0));
+        if constexpr (!PAIR_EMPTY) {
+          if (leader) ptx::mma_commit(bEmpty(0));
+        }
       }
       for (int j = 0; ok && j < n; ++j) {
         const int iv = 2 * j + 1, sv = iv % NSLOT;  // V_j
         const int ik = 2 * j + 2, sk = ik % NSLOT;  // K_{j+1}
         const bool more = j + 1 < n;
-        ok = wait_bar(bPair(j % NPB), (j / NPB) & 1, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);  // V_j, K_{j+1}
+        ok = mma_wait<CONV>(bPair(j % NPB), (j / NPB) & 1, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);  // V_j, K_{j+1}
         if (!ok) break;
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
           const int nX = x == 0 ? nA : nB;
           if (j < nX) {
-            ok = wait_bar(bPfull(x), j & 1, abort_flag, p.watchdog_ns, WD_MMA_P_FULL);
+            ok = mma_wait<CONV>(bPfull(x), j & 1, abort_flag, p.watchdog_ns, WD_MMA_P_FULL);
             if (!ok) break;
             ptx::tc_fence_after();
             issue_pv(x, sv, j > 0);
           }
-          if (x == 1) {
+          if (x == 1 && leader) {
             if constexpr (PAIR_EMPTY)
               ptx::mma_commit(bEmpty(j % NPE));  // K_j (its S MMAs came earlier) and V_j, once P V_B(j) is done
             else
@@ -515,13 +532,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (!ok) break;
         if constexpr (!PAIR_EMPTY) {
-          if (more) ptx::mma_commit(bEmpty(sk));
+          if (more && leader) ptx::mma_commit(bEmpty(sk));
         }
       }
-      if (ok) ptx::mma_commit(bOfinal);
+      if (ok && leader) ptx::mma_commit(bOfinal);
       // every MMA issued has finished before TMEM is freed (the softmax may
       // have given up without waiting for o_final)
-      ptx::mma_commit(bDrain);
+      if (leader) ptx::mma_commit(bDrain);
       drain_wait(bDrain, 0, DRAIN_NS);
     }
   }
@@ -1351,6 +1368,12 @@ __global__ void __launch_bounds__(MERGE_THREADS)
                                                pack2<BF16>(a[4] * inv, a[5] * inv), pack2<BF16>(a[6] * inv, a[7] * inv));
 }
 
+}  // namespace fa
+
+#include "fa_persistent.cuh"
+
+namespace fa {
+
 // =============================================================== host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -1416,6 +1439,12 @@ static std::atomic<int> g_dev_ok[MAX_DEVICES];
 static std::atomic<int> g_dev_sms[MAX_DEVICES];
 static std::atomic<int> g_attr_set[MAX_DEVICES][4];
 static std::atomic<int> g_sk_attr_set[MAX_DEVICES][8];
+static std::atomic<int> g_pk_attr_set[MAX_DEVICES][4];
+// Kernel selection for testing and measurement (fa_debug_force_path): 0 the
+// library's choice, 1 the one-shot kernel (also for calls with a workspace),
+// 2 the persistent kernel (over whole units without a workspace; for every
+// split-KV schedule with one).
+static std::atomic<int> g_force_path{0};
 static std::atomic<int> g_attr256_set[MAX_DEVICES][2];
 
 static int check_device(int* dev_out) {
@@ -1438,7 +1467,7 @@ static int check_device(int* dev_out) {
     g_dev_sms[dev].store(sms > 0 ? sms : 1);
     if (major != 10 || minor != 3) st = -FA_ERR_DEVICE;
     else if ((unsigned)optin < Layout<128>::REQUEST || (unsigned)optin < SkLayout<128>::REQUEST ||
-             (unsigned)optin < Layout256::REQUEST)
+             (unsigned)optin < Layout256::REQUEST || (unsigned)optin < PkLayout<128>::REQUEST)
       st = -FA_ERR_SMEM;
     else st = 1;
     g_dev_ok[dev].store(st);
@@ -1476,6 +1505,11 @@ struct Paged {
   const int* table;
   int page_size, max_pages, num_blocks;
 };
+
+template <int HD, bool BF16>
+static int launch_pk(const void* q, const void* k, const void* v, void* o, int hd, int B, int Hq, int Hkv, int Sq, int Skv,
+                     int kv_cap, int causal, float scale, float4* ws_o, float* ws_ml, cudaStream_t stream, int dev,
+                     const Paged* pg = nullptr, float* lse = nullptr);
 
 // K/V maps for the producers, and the paged fields of Params.  Contiguous:
 // Skv rows per sequence with a batch stride of kv_cap rows (the tail maps
@@ -1649,6 +1683,13 @@ static int run(bool bf16, const void* q, const void* k, const void* v, void* o, 
   if (kernel_hd(hd) == 256)
     return bf16 ? launch256<true>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev)
                 : launch256<false>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev);
+  if (g_force_path.load() == 2) {  // the persistent kernel over whole units (testing and measurement)
+    if (kernel_hd(hd) == 128)
+      return bf16 ? launch_pk<128, true>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, nullptr, nullptr, st, dev)
+                  : launch_pk<128, false>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, nullptr, nullptr, st, dev);
+    return bf16 ? launch_pk<64, true>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, nullptr, nullptr, st, dev)
+                : launch_pk<64, false>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, nullptr, nullptr, st, dev);
+  }
   if (kernel_hd(hd) == 128)
     return bf16 ? launch<128, true>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev)
                 : launch<128, false>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev);
@@ -1881,21 +1922,100 @@ static int launch_sk(const void* q, const void* k, const void* v, void* o, int h
   prm.watchdog_ns = g_watchdog_ns.load();
   SkSchedule sc;
   get_schedule(prm, g_dev_sms[dev].load(), &sc);
-  auto kern = sc.one_seg ? fa_prefill_sk_kernel<HD, BF16, true> : fa_prefill_sk_kernel<HD, BF16, false>;
-  if (!sk_attr(kern, dev, (HD == 128 ? 2 : 0) + (BF16 ? 1 : 0) + (sc.one_seg ? 4 : 0), SL::REQUEST)) return FA_ERR_SMEM;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  sp.ws_o = reinterpret_cast<float4*>(base);
+  sp.ws_ml = reinterpret_cast<float*>(base + SL::WS_O_BYTES);
+  // CTAs that run several segments: the persistent kernel (its epilogue
+  // warpgroup overlaps each segment's output with the next segment's steps)
+  if (!sc.one_seg || g_force_path.load() == 2)
+    return launch_pk<HD, BF16>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, kv_cap, causal, scale, sp.ws_o, sp.ws_ml, stream, dev,
+                               pg, lse);
+  auto kern = fa_prefill_sk_kernel<HD, BF16, true>;
+  if (!sk_attr(kern, dev, (HD == 128 ? 2 : 0) + (BF16 ? 1 : 0) + 4, SL::REQUEST)) return FA_ERR_SMEM;
   std::memcpy(sp.su, sc.su, sizeof(int) * (sc.G + 1));
   std::memcpy(sp.sj, sc.sj, sizeof(int) * (sc.G + 1));
   std::memcpy(sp.pf, sc.pf, sizeof(short) * sc.G);
   std::memcpy(sp.ph, sc.ph, sizeof(short) * sc.G);
-  uint8_t* base = static_cast<uint8_t*>(ws);
-  sp.ws_o = reinterpret_cast<float4*>(base);
-  sp.ws_ml = reinterpret_cast<float*>(base + SL::WS_O_BYTES);
   if (launch_pdl(kern, dim3(static_cast<unsigned>(sc.G)), dim3(NUM_THREADS), SL::REQUEST, stream, mq, mk, mv, mo, mkt,
                  mvt, sp) != cudaSuccess) {
     (void)cudaGetLastError();
     return FA_ERR_LAUNCH;
   }
   return launch_merge<HD, BF16>(sc, prm, sp.ws_o, sp.ws_ml, stream);
+}
+
+// The persistent kernel.  Without a workspace (ws_o == nullptr) every CTA
+// takes whole units in snake order (grid = min(SMs, units)); with one, the
+// stream-K ranges of the split-KV schedule, then the merge of the split units.
+template <int HD, bool BF16>
+static int launch_pk(const void* q, const void* k, const void* v, void* o, int hd, int B, int Hq, int Hkv, int Sq, int Skv,
+                     int kv_cap, int causal, float scale, float4* ws_o, float* ws_ml, cudaStream_t stream, int dev,
+                     const Paged* pg, float* lse) {
+  using PL = PkLayout<HD>;
+  EncodeTiledFn enc = encoder();
+  if (!enc) return FA_ERR_LAUNCH;
+  CUtensorMap mq, mk, mv, mkt, mvt;
+  Params pkv;
+  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, hd, Sq) ||
+      !encode_kv(&mk, &mv, &mkt, &mvt, enc, k, v, BF16, B, Skv, kv_cap, Hkv, hd, pg, &pkv))
+    return FA_ERR_LAUNCH;
+  PkParams sp;
+  std::memset(&sp, 0, sizeof(sp));
+  Params& prm = sp.p;
+  prm.o = static_cast<uint16_t*>(o);
+  prm.hd = hd;
+  prm.B = B;
+  prm.Hq = Hq;
+  prm.Hkv = Hkv;
+  prm.Sq = Sq;
+  prm.Skv = Skv;
+  prm.G = Hq / Hkv;
+  prm.n_qtiles = (Sq + BM - 1) / BM;
+  prm.pair_heads = (prm.G % 2 == 0) ? 1 : 0;
+  prm.causal = causal ? 1 : 0;
+  prm.sl2 = scale * 1.4426950408889634f;
+  prm.block_table = pkv.block_table;
+  prm.page_size = pkv.page_size;
+  prm.max_pages = pkv.max_pages;
+  prm.num_blocks = pkv.num_blocks;
+  prm.last_page = pkv.last_page;
+  prm.lse = lse;
+  prm.watchdog_ns = g_watchdog_ns.load();
+  const long long nu = unit_count_of(prm);
+  if (nu > 0x7FFFFFFFLL) return FA_ERR_UNSUPPORTED;
+  sp.n_units = static_cast<int>(nu);
+  const int sms = g_dev_sms[dev].load();
+  auto kern = fa_prefill_pk_kernel<HD, BF16>;
+  const int aslot = (HD == 128 ? 2 : 0) + (BF16 ? 1 : 0);
+  if (g_pk_attr_set[dev][aslot].load() == 0) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PL::REQUEST) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return FA_ERR_SMEM;
+    }
+    g_pk_attr_set[dev][aslot].store(1);
+  }
+  SkSchedule sc;
+  int grid;
+  if (ws_o) {
+    get_schedule(prm, sms, &sc);
+    sp.ranges = 1;
+    grid = sc.G;
+    std::memcpy(sp.su, sc.su, sizeof(int) * (sc.G + 1));
+    std::memcpy(sp.sj, sc.sj, sizeof(int) * (sc.G + 1));
+    std::memcpy(sp.pf, sc.pf, sizeof(short) * sc.G);
+    std::memcpy(sp.ph, sc.ph, sizeof(short) * sc.G);
+    sp.ws_o = ws_o;
+    sp.ws_ml = ws_ml;
+  } else {
+    sp.ranges = 0;
+    grid = static_cast<int>(std::min<long long>(nu, std::max(1, sms)));
+  }
+  if (launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(PK_THREADS), PL::REQUEST, stream, mq, mk, mv, mkt, mvt,
+                 sp) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return FA_ERR_LAUNCH;
+  }
+  return ws_o ? launch_merge<HD, BF16>(sc, prm, sp.ws_o, sp.ws_ml, stream) : FA_OK;
 }
 
 // Attention over a K/V cache of kv_cap rows per sequence of which the first
@@ -2037,6 +2157,13 @@ static int run_ws(bool bf16, const void* q, const void* k, const void* v, void* 
   const int ds = check_device(&dev);
   if (ds != FA_OK) return ds;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (g_force_path.load() == 1) {
+    if (kernel_hd(hd) == 128)
+      return bf16 ? launch<128, true>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev)
+                  : launch<128, false>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev);
+    return bf16 ? launch<64, true>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev)
+                : launch<64, false>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, st, dev);
+  }
   if (kernel_hd(hd) == 128)
     return bf16 ? launch_sk<128, true>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, ws, st, dev)
                 : launch_sk<128, false>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, Skv, causal, scale, ws, st, dev);
@@ -2123,8 +2250,10 @@ static int launch_sk_static(const void* q, const void* k, const void* v, void* o
   std::memcpy(sp.ph, sc.ph, sizeof(short) * sc.G);
   sp.ws_ml = reinterpret_cast<float*>(base);
   sp.ws_o = reinterpret_cast<float4*>(base + STATIC_O_OFF);
-  auto kern = sc.one_seg ? fa_prefill_sk_kernel<HD, BF16, true> : fa_prefill_sk_kernel<HD, BF16, false>;
-  if (!sk_attr(kern, dev, (HD == 128 ? 2 : 0) + (BF16 ? 1 : 0) + (sc.one_seg ? 4 : 0), SL::REQUEST)) return FA_ERR_SMEM;
+  if (!sc.one_seg)  // as the workspace path: multi-segment CTAs on the persistent kernel
+    return launch_pk<HD, BF16>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, kv_cap, causal, scale, sp.ws_o, sp.ws_ml, stream, dev);
+  auto kern = fa_prefill_sk_kernel<HD, BF16, true>;
+  if (!sk_attr(kern, dev, (HD == 128 ? 2 : 0) + (BF16 ? 1 : 0) + 4, SL::REQUEST)) return FA_ERR_SMEM;
   EncodeTiledFn enc = encoder();
   if (!enc) return FA_ERR_LAUNCH;
   // the maps describe the caller's head width hd (<= HD): TMA zero-fills the
@@ -2312,6 +2441,12 @@ extern "C" int fa_debug_status_clear(void) {
     (void)cudaGetLastError();
     return FA_ERR_DEVICE;
   }
+  return FA_OK;
+}
+
+extern "C" int fa_debug_force_path(int path) {
+  if (path < 0 || path > 2) return FA_ERR_INVALID_ARG;
+  fa::g_force_path.store(path);
   return FA_OK;
 }
 

@@ -78,6 +78,7 @@
  *   fa_prefill_ws_static             split-KV with library-owned scratch
  *   fa_status_string, fa_smem_bytes, fa_debug_status(_clear)  diagnostics
  *   fa_debug_set_watchdog_ns         testing hook: the kernels' wait limit
+ *   fa_debug_force_path              testing hook: which kernel runs
  *   fa_debug_schedule                the split-KV work split for a shape
  */
 #ifndef FA_PREFILL_H
@@ -127,12 +128,15 @@ int fa_prefill_bf16(const void* q, const void* k, const void* v, void* o,
 
 /*
  * fa_prefill_ws / fa_prefill_ws_bf16 -- the same operation computed by a
- * load-balanced split-KV kernel: at most one CTA per SM.  With no more
+ * load-balanced split-KV schedule: at most one CTA per SM.  With no more
  * query-tile pairs than SMs, each pair is cut into near-equal pieces of its
- * KV steps and every CTA computes one piece; with more pairs, the CTAs are
- * persistent and each takes an equal contiguous share of all (query-tile
- * pair, KV tile) steps ("stream-K").  Either way short prompts, single heads
- * and causal rows of very different lengths keep every SM busy.  A
+ * KV steps and every CTA computes one piece (the split-KV kernel); with more
+ * pairs, the CTAs are persistent and each takes an equal contiguous share of
+ * all (query-tile pair, KV tile) steps ("stream-K", the persistent kernel,
+ * whose epilogue warpgroup writes one segment's output while the next
+ * segment's steps run).  Either way short prompts, single heads, causal rows
+ * of very different lengths and grids of a few more pairs than SMs keep
+ * every SM busy.  A
  * query-tile pair whose KV steps are split between CTAs is merged
  * by a second, short kernel enqueued behind the first (programmatic dependent
  * launch), over the whole GPU and in a fixed order (results are
@@ -366,9 +370,12 @@ unsigned int fa_smem_bytes(int hd);
 /*
  * fa_debug_status -- the kernel watchdog word of the current device: 0 when
  * no kernel has reported a problem since the last clear, otherwise a code
- * (bits 0-7: which wait gave up -- or 12, a split piece the schedule gave no
- * workspace slot (not expected), 32, a cache-append position out of
- * range (fa_kv_append), or 33, a block-table entry outside the pool
+ * (bits 0-7: which wait gave up -- 1 to 8 in the one-shot and split-KV
+ * kernels, 14 to 16 the persistent kernel's epilogue, O-free and (m, l)
+ * hand-off waits -- or 12, a split piece the schedule gave no workspace slot
+ * (not expected), 17, a persistent kernel whose shared memory was not
+ * 1024-byte aligned (nothing run; not expected), 32, a cache-append position
+ * out of range (fa_kv_append), or 33, a block-table entry outside the pool
  * (fa_prefill_paged); bits 8-31: the CTA or token index, saturated).  A
  * pipeline wait that does not complete within the watchdog limit records its
  * code here, makes its CTA skip its remaining work and exit cleanly (no trap),
@@ -391,6 +398,19 @@ int fa_debug_status_clear(void);
  * process-wide.  Returns FA_OK.
  */
 int fa_debug_set_watchdog_ns(unsigned long long ns);
+
+/*
+ * fa_debug_force_path -- a testing and measurement hook: the kernel that calls
+ * made after it run on, process-wide.  0: the library's own choice (the
+ * default); 1: the one-shot kernel, also for calls given a workspace (no
+ * split); 2: the persistent kernel -- over whole query-tile pairs, each CTA
+ * taking pairs in snake order, for calls without a workspace, and for every
+ * split-KV schedule (not only multi-segment ones) for calls with one.  Heads
+ * wider than 128 always run on the one-shot kernel.  The result is the same
+ * within the parity tolerance whatever the path.  Host-only.  Returns FA_OK,
+ * or FA_ERR_INVALID_ARG for another value (nothing changed).
+ */
+int fa_debug_force_path(int path);
 
 /*
  * fa_debug_schedule -- the work split fa_prefill_ws launches for a shape on

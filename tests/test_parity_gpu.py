@@ -43,9 +43,14 @@ def _inputs(B, Hq, Hkv, Sq, Skv, hd, dtype="f16", seed=0, q_std=1.0, k_std=1.0, 
     return w, W.make_inputs(w)
 
 
-@pytest.fixture(params=[False, True], ids=["oneshot", "streamk"])
+@pytest.fixture(params=[False, True, "persistent", "persistent_ws"],
+                ids=["oneshot", "splitkv", "persistent", "persistent_ws"])
 def split(request):
-    """Run a parity test through the one-shot kernel and the stream-K kernel."""
+    """Run a parity test through the one-shot kernel, the split-KV path as the
+    library routes it (one piece per CTA on the stream-K kernel, several
+    segments per CTA on the persistent kernel), and the persistent kernel
+    forced: over whole units without a workspace, and over the split-KV
+    schedule with one."""
     return request.param
 
 
@@ -53,7 +58,14 @@ def _run_gpu(q, k, v, causal, scale, fill=float("nan"), split=False):
     fa = _fa()
     dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
     out = torch.full_like(dq, fill)  # NaN-prefilled: an unwritten element fails parity
-    fa.attention(dq, dk, dv, causal=causal, scale=scale, out=out, split=split)
+    if isinstance(split, str):
+        fa.debug_force_path("persistent")
+        try:
+            fa.attention(dq, dk, dv, causal=causal, scale=scale, out=out, split=split == "persistent_ws")
+        finally:
+            fa.debug_force_path("auto")
+    else:
+        fa.attention(dq, dk, dv, causal=causal, scale=scale, out=out, split=split)
     torch.cuda.synchronize()
     assert fa.debug_status() == 0, f"kernel watchdog fired: {fa.debug_status():#x}"
     return out.cpu()
@@ -236,7 +248,7 @@ def test_workload_reduced_full_compare(idx, split):
     size the oracle finishes in seconds, spanning several tiles and a ragged tail."""
     w = W.WORKLOADS[idx]
     if split and w.hd == 256:
-        pytest.skip("split-KV takes hd 64 and 128")
+        pytest.skip("split-KV and the persistent kernel take hd 64 and 128")
     if w.Sq == w.Skv:
         small = w.with_(B=1, Hq=min(w.Hq, 8), Hkv=min(w.Hkv, 8) if w.Hq == w.Hkv else 2,
                         Sq=w.Sq % 128 + 2 * 128 if w.Sq % 128 else 3 * 128 - 1,
@@ -256,7 +268,7 @@ def test_workload_full_size_sampled_rows(idx, split):
     against the oracle computed row by row; plus whole-tensor properties."""
     w = W.WORKLOADS[idx]
     if split and w.hd == 256:
-        pytest.skip("split-KV takes hd 64 and 128")
+        pytest.skip("split-KV and the persistent kernel take hd 64 and 128")
     q, k, v = W.make_inputs(w)
     got = _run_gpu(q, k, v, w.causal, w.scale, split=split)
     assert torch.isfinite(got).all()

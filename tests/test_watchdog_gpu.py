@@ -22,8 +22,9 @@ from causal_prefill_flash_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 
-# producer empty, MMA Q / K-V / P, softmax S / O: the codes of the pipeline waits
-WAIT_CODES = {1, 3, 4, 5, 7, 8}
+# producer empty, MMA Q / K-V / P, softmax S / O, and the persistent kernel's
+# epilogue O, MMA O-empty and softmax (m, l) hand-off: the pipeline-wait codes
+WAIT_CODES = {1, 3, 4, 5, 7, 8, 14, 15, 16}
 WD_DRAIN = 9
 TOL = {"f16": 2e-3, "bf16": 8e-3}
 
@@ -56,6 +57,8 @@ CASES = [  # (name, B, Hq, Hkv, S, hd, dtype, path)
     ("hd256", 1, 4, 2, 900, 256, "bf16", "oneshot"),
     ("split_kv", 1, 8, 2, 2000, 128, "f16", "split"),
     ("paged", 2, 8, 4, 1300, 128, "f16", "paged"),
+    ("persistent_hd128", 1, 32, 8, 2200, 128, "bf16", "persistent"),
+    ("persistent_ws_hd64", 2, 16, 4, 2300, 64, "f16", "persistent_ws"),
 ]
 
 
@@ -67,6 +70,15 @@ def test_waits_that_run_out_are_reported_and_leave_the_context_usable(case):
     q, k, v = W.make_inputs(w)
     if path == "paged":
         call = _paged_call(fa, q, k, v, 256, w)
+    elif path.startswith("persistent"):
+        dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
+
+        def call(out):
+            fa.debug_force_path("persistent")
+            try:
+                fa.attention(dq, dk, dv, causal=True, scale=w.scale, out=out, split=path == "persistent_ws")
+            finally:
+                fa.debug_force_path("auto")
     else:
         dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
         call = lambda out: fa.attention(dq, dk, dv, causal=True, scale=w.scale, out=out, split=(path == "split"))
