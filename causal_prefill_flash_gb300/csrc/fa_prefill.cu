@@ -729,19 +729,17 @@ namespace fa {
 // ================================================ stream-K (split-KV) kernel
 //
 // The one-shot kernel above gives every CTA whole query-tile pairs, so a grid
-// with few or uneven pairs (short prompts, one head, causal rows of very
-// different lengths) leaves SMs idle and pays the pipeline fill and drain once
-// per CTA.  This kernel runs at most one CTA per SM over the whole iteration
-// space -- (query-tile pair, KV tile) steps, pairs longest first.  With no
-// more pairs than CTAs each pair is cut into near-equal pieces and every CTA
-// computes one (the ONE_SEG instantiation: a single step loop, as in the
-// one-shot kernel); otherwise the CTAs are persistent and each takes an equal
-// contiguous range of steps.  A pair whose steps straddle a range boundary
-// is computed in pieces: every piece leaves its unnormalised O, running max m
-// and sum l in a workspace slot the host assigned, and a second, short kernel
-// (fa_sk_merge_kernel, chained by programmatic dependent launch) combines
-// each split pair's pieces over the whole GPU in a fixed order, so results
-// are deterministic.  No CTA waits on another.
+// with few pairs (a short chunk over a long context, one head) leaves SMs
+// idle.  With no more pairs than SMs, the split-KV schedule cuts each pair
+// into near-equal pieces of its KV steps, one per CTA, and this kernel runs
+// them: every CTA computes one segment (unit u, KV steps [jb, je)) with the
+// one-shot kernel's single step loop.  (Schedules with more pairs than SMs,
+// where a CTA runs several segments, go to the persistent kernel in
+// fa_persistent.cuh.)  A split pair's pieces each leave their unnormalised O,
+// running max m and sum l in a workspace slot the host assigned, and a
+// second, short kernel (fa_sk_merge_kernel, chained by programmatic dependent
+// launch) combines them over the whole GPU in a fixed order, so results are
+// deterministic.  No CTA waits on another.
 
 constexpr int SK_MAX_CTAS = 256;
 // The segment loop keeps more state in the control warps than the one-shot
@@ -773,9 +771,9 @@ struct SkLayout {
   // thread writes its row straight from registers (or its piece to the
   // workspace), and the ring keeps the one-shot kernel's depth.
   static constexpr int NSLOT = HD == 128 ? 5 : 8;
-  // q_full, q_empty, full[NSLOT] (ONE_SEG: pair barriers, the first NPB), empty[NSLOT], s_full[2],
-  // p_full[2], o_final[2], drain
-  static constexpr uint32_t NUM_BARS = 2 + 2 * NSLOT + 2 + 2 + 2 + 1;
+  // q_full, full[NSLOT] (pair barriers: the first NPB), empty[NSLOT], s_full[2], p_full[2],
+  // o_final[2], drain
+  static constexpr uint32_t NUM_BARS = 1 + 2 * NSLOT + 2 + 2 + 2 + 1;
   static constexpr uint32_t OFF_BAR = L::OFF_RING + NSLOT * L::SLOT_BYTES;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr uint32_t BYTES = OFF_MISC + 16;
@@ -833,7 +831,7 @@ __host__ __device__ __forceinline__ UnitGeo unit_geo(const Params& p, int u) {
   return w;
 }
 
-template <int HD, bool BF16, bool ONE_SEG>
+template <int HD, bool BF16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fa_prefill_sk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -857,30 +855,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t sRing = sbase + L::OFF_RING;
   const uint32_t bar = sbase + SL::OFF_BAR;
   const uint32_t bQfull = bar;
-  const uint32_t bQempty = bar + 8u;
-  auto bFull = [&](int s) { return bar + 8u * (2 + s); };
-  auto bEmpty = [&](int s) { return bar + 8u * (2 + NSLOT + s); };
-  auto bSfull = [&](int x) { return bar + 8u * (2 + 2 * NSLOT + x); };
-  auto bPfull = [&](int x) { return bar + 8u * (4 + 2 * NSLOT + x); };
-  auto bOfinal = [&](int x) { return bar + 8u * (6 + 2 * NSLOT + x); };
-  const uint32_t bDrain = bar + 8u * (8 + 2 * NSLOT);
+  auto bFull = [&](int s) { return bar + 8u * (1 + s); };
+  auto bEmpty = [&](int s) { return bar + 8u * (1 + NSLOT + s); };
+  auto bSfull = [&](int x) { return bar + 8u * (1 + 2 * NSLOT + x); };
+  auto bPfull = [&](int x) { return bar + 8u * (3 + 2 * NSLOT + x); };
+  auto bOfinal = [&](int x) { return bar + 8u * (5 + 2 * NSLOT + x); };
+  const uint32_t bDrain = bar + 8u * (7 + 2 * NSLOT);
   uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + SL::OFF_MISC);
   volatile uint32_t* abort_flag = misc + 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int cta = static_cast<int>(blockIdx.x);
-  const int u_beg = sp.su[cta], j_beg = sp.sj[cta];
-  const int u_end = sp.su[cta + 1], j_end = sp.sj[cta + 1];
-  // the segments of this CTA: (unit u, steps [jb, je)), u from u_beg; the last
-  // one may stop before the unit's end (at the next CTA's start)
-  auto in_range = [&](int u, int jb) { return u < u_end || (u == u_end && jb < j_end); };
+  // this CTA's one segment: unit u, KV steps [jb, je) (it ends where the next
+  // CTA starts, or at the unit's end)
+  const int u = sp.su[cta], jb = sp.sj[cta];
+  const UnitGeo w = unit_geo(p, u);
+  const int je = (sp.su[cta + 1] == u) ? sp.sj[cta + 1] : w.n;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bQfull, 1);
-    ptx::mbar_init(bQempty, 1);
     for (int s = 0; s < NSLOT; ++s) {
-      ptx::mbar_init(bFull(s), ONE_SEG && s < NPB ? 2 : 1);  // pair barriers: one arrival per load
+      ptx::mbar_init(bFull(s), s < NPB ? 2 : 1);  // pair barriers (the first NPB): one arrival per load
       ptx::mbar_init(bEmpty(s), 1);
     }
     for (int x = 0; x < 2; ++x) {
@@ -917,16 +913,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::prefetch_tmap(&tmKt);
         ptx::prefetch_tmap(&tmVt);
       }
-      int g = 0;   // loads issued into the ring
-      int nq = 0;  // segments whose Q was loaded
+      int g = 0;  // loads issued into the ring: K_jb, then pairs (V_t, K_t+1)
       bool ok = true;
-      for (int u = u_beg, jb = j_beg; ok && in_range(u, jb); ++u, jb = 0) {
-        const UnitGeo w = unit_geo(p, u);
-        const int je = (u == u_end) ? j_end : w.n;
-        if (je <= jb) continue;  // nothing to stream (the softmax writes zeros)
-        if (nq > 0) ok = wait_bar(bQempty, (nq - 1) & 1, abort_flag, p.watchdog_ns, WD_PRODUCER_EMPTY);
-        if (!ok) break;
-        ptx::mbar_arrive_expect_tx(bQfull, L::Q_BYTES * (w.has1 ? 2u : 1u) + (ONE_SEG ? L::SLOT_BYTES : 0u));
+      if (je > jb) {  // else nothing to stream (the softmax writes zeros)
+        ptx::mbar_arrive_expect_tx(bQfull, L::Q_BYTES * (w.has1 ? 2u : 1u) + L::SLOT_BYTES);
 #pragma unroll
         for (int c = 0; c < (int)L::KCH; ++c)
           ptx::tma_load_4d(sQ + c * (BM * 128), &tmQ, bQfull, c * 64, w.hq0, w.q00, w.b);
@@ -934,16 +924,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int c = 0; c < (int)L::KCH; ++c)
             ptx::tma_load_4d(sQ + L::Q_BYTES + c * (BM * 128), &tmQ, bQfull, c * 64, w.hq1, w.q01, w.b);
-        }
-        ++nq;
-        // warm L2 with the next segment's Q: its load then waits for L2, not HBM
-        if (in_range(u + 1, 0)) {
-          const UnitGeo w2 = unit_geo(p, u + 1);
-#pragma unroll
-          for (int c = 0; c < (int)L::KCH; ++c) {
-            ptx::tma_prefetch_l2_4d(&tmQ, c * 64, w2.hq0, w2.q00, w2.b);
-            if (w2.has1) ptx::tma_prefetch_l2_4d(&tmQ, c * 64, w2.hq1, w2.q01, w2.b);
-          }
         }
         int page = -1, blk = 0;  // paged K/V: the pool block of the current page
         for (int i = 2 * jb; i < 2 * je; ++i, ++g) {
@@ -968,18 +948,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bat = blk;
             tail = pg == p.last_page;
           }
-          uint32_t fb = bFull(s);
-          if constexpr (ONE_SEG) {  // g counts this segment's loads: K_jb, then pairs (V, K)
-            const int pj = (g - 1) >> 1;
-            fb = g == 0 ? bQfull : bFull(pj % NPB);
-            if ((g & 1) && pj >= NPB) {  // pair pj reuses pair pj-NPB's barrier
-              ok = wait_bar(fb, ((pj - NPB) / NPB) & 1, abort_flag, p.watchdog_ns, WD_PRODUCER_EMPTY);
-              if (!ok) break;
-            }
-            if (g > 0) ptx::mbar_arrive_expect_tx(fb, L::SLOT_BYTES);
-          } else {
-            ptx::mbar_arrive_expect_tx(fb, L::SLOT_BYTES);
+          const int pj = (g - 1) >> 1;  // pair of load g (V_pj, K_pj+1); K_jb comes with Q
+          const uint32_t fb = g == 0 ? bQfull : bFull(pj % NPB);
+          if ((g & 1) && pj >= NPB) {  // pair pj reuses pair pj-NPB's barrier
+            ok = wait_bar(fb, ((pj - NPB) / NPB) & 1, abort_flag, p.watchdog_ns, WD_PRODUCER_EMPTY);
+            if (!ok) break;
           }
+          if (g > 0) ptx::mbar_arrive_expect_tx(fb, L::SLOT_BYTES);
           const CUtensorMap* m = (i & 1) ? (tail ? &tmVt : &tmV) : (tail ? &tmKt : &tmK);
 #pragma unroll
           for (int c = 0; c < (int)L::KCH; ++c)
@@ -987,20 +962,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       // a pair whose K was not issued (the last V, or a CTA that gave up)
-      if (ONE_SEG && g >= 2 && (g & 1) == 0) ptx::mbar_arrive(bFull(((g - 2) >> 1) % NPB));
+      if (g >= 2 && (g & 1) == 0) ptx::mbar_arrive(bFull(((g - 2) >> 1) % NPB));
       // every copy issued has landed before the CTA exits (as in the one-shot kernel)
-      if (nq > 0) drain_wait(bQfull, (nq - 1) & 1, DRAIN_NS);
-      if constexpr (ONE_SEG) {
-        const int npairs = g / 2;  // pairs armed
-        for (int b = 0; b < NPB && b < npairs; ++b) {
-          const int last = b + NPB * ((npairs - 1 - b) / NPB);
-          drain_wait(bFull(b), (last / NPB) & 1, DRAIN_NS);
-        }
-      } else {
-        for (int s = 0; s < NSLOT && s < g; ++s) {
-          const int last = s + NSLOT * ((g - 1 - s) / NSLOT);
-          drain_wait(bFull(s), (last / NSLOT) & 1, DRAIN_NS);
-        }
+      if (je > jb) drain_wait(bQfull, 0, DRAIN_NS);
+      const int npairs = g / 2;  // pairs armed
+      for (int b = 0; b < NPB && b < npairs; ++b) {
+        const int last = b + NPB * ((npairs - 1 - b) / NPB);
+        drain_wait(bFull(b), (last / NPB) & 1, DRAIN_NS);
       }
     } else if (warp == MMA_WARP && lane == 0) {
       // ------------------------------------------------------- MMA issuer
@@ -1027,50 +995,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ptx::mma_f16_ts(d, a + kk * 8, ptx::sdesc_join(v + kk * ((16 * 128) >> 4), DHI), IDESC_O,
                           (acc || kk > 0) ? 1u : 0u);
       };
-      int g = 0, nq = 0, cnt0 = 0, cnt1 = 0;
       bool ok = true;
-      // With one segment per CTA the loop runs once, and the compiler lays
-      // out the step loop as in the one-shot kernel (measured: the nested
-      // form issues ~15 % slower).
-      for (int u = u_beg, jb = j_beg; ok && (ONE_SEG ? u == u_beg : in_range(u, jb)); ++u, jb = 0) {
-        const UnitGeo w = unit_geo(p, u);
-        const int je = (u == u_end) ? j_end : w.n;
-        if (je <= jb) continue;
+      if (je > jb) {
         const int nseg = je - jb;
         const int nAs = max(0, min(je, w.nA) - jb);  // tiles of A / B in this segment
         const int nBs = max(0, min(je, w.nB) - jb);
-        ok = wait_bar(bQfull, nq & 1, abort_flag, p.watchdog_ns, WD_MMA_Q);
-        if (!ok) break;
-        const int gK = g;  // ring index of K_jb; V_(jb+t) = gK + 2t + 1, K_(jb+t) = gK + 2t
-        if constexpr (!ONE_SEG) {  // one segment: K_jb came with Q
-          ok = wait_bar(bFull(gK % NSLOT), (gK / NSLOT) & 1, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);
-          if (!ok) break;
+        ok = wait_bar(bQfull, 0, abort_flag, p.watchdog_ns, WD_MMA_Q);  // Q and K_jb
+        if (ok) {
+          ptx::tc_fence_after();
+          if (nAs > 0) issue_s(0, 0);
+          if (nBs > 0) issue_s(1, 0);
+          ptx::mma_commit(bEmpty(0));
         }
-        ptx::tc_fence_after();
-        if (nAs > 0) issue_s(0, gK % NSLOT);
-        if (nBs > 0) issue_s(1, gK % NSLOT);
-        ptx::mma_commit(bEmpty(gK % NSLOT));
-        if (nseg == 1) ptx::mma_commit(bQempty);
+        // ring index of V_(jb+t) is 2t + 1, of K_(jb+t+1) 2t + 2; both on pair barrier t % NPB
         for (int t = 0; ok && t < nseg; ++t) {
-          const int iv = gK + 2 * t + 1, sv = iv % NSLOT;
-          const int ik = gK + 2 * t + 2, sk = ik % NSLOT;
+          const int sv = (2 * t + 1) % NSLOT;
+          const int sk = (2 * t + 2) % NSLOT;
           const bool more = t + 1 < nseg;
-          if constexpr (ONE_SEG) {
-            ok = wait_bar(bFull(t % NPB), (t / NPB) & 1, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);  // V_t, K_t+1
-            if (!ok) break;
-          } else {
-            ok = wait_bar(bFull(sv), (iv / NSLOT) & 1, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);
-            if (!ok) break;
-            if (more) {
-              ok = wait_bar(bFull(sk), (ik / NSLOT) & 1, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);
-              if (!ok) break;
-            }
-          }
+          ok = wait_bar(bFull(t % NPB), (t / NPB) & 1, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);  // V_t, K_t+1
+          if (!ok) break;
 #pragma unroll
           for (int x = 0; x < 2; ++x) {
             const int nXs = x == 0 ? nAs : nBs;
             if (t < nXs) {
-              ok = wait_bar(bPfull(x), ((x == 0 ? cnt0 : cnt1) + t) & 1, abort_flag, p.watchdog_ns, WD_MMA_P_FULL);
+              ok = wait_bar(bPfull(x), t & 1, abort_flag, p.watchdog_ns, WD_MMA_P_FULL);
               if (!ok) break;
               ptx::tc_fence_after();
               issue_pv(x, sv, t > 0);
@@ -1079,18 +1027,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (more && t + 1 < nXs) issue_s(x, sk);
           }
           if (!ok) break;
-          if (more) {
-            ptx::mma_commit(bEmpty(sk));
-            if (t + 2 == nseg) ptx::mma_commit(bQempty);  // the segment's last S MMAs are issued
-          }
+          if (more) ptx::mma_commit(bEmpty(sk));
         }
-        if (!ok) break;
-        if (nAs > 0) ptx::mma_commit(bOfinal(0));
-        if (nBs > 0) ptx::mma_commit(bOfinal(1));
-        g = gK + 2 * nseg;
-        cnt0 += nAs;
-        cnt1 += nBs;
-        ++nq;
+        if (ok && nAs > 0) ptx::mma_commit(bOfinal(0));
+        if (ok && nBs > 0) ptx::mma_commit(bOfinal(1));
       }
       // every MMA issued has finished before TMEM is freed
       ptx::mma_commit(bDrain);
@@ -1110,9 +1050,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int cnt = 0;   // tiles processed (s_full / p_full phases)
     int ocnt = 0;  // segments with tiles of x (o_final phases)
     bool ok = true;
-    for (int u = u_beg, jb = j_beg; ok && in_range(u, jb); ++u, jb = 0) {
-      const UnitGeo w = unit_geo(p, u);
-      const int je = (u == u_end) ? j_end : w.n;
+    do {
       const bool first = jb == 0;
       const bool last = je >= w.n;
       const int q0 = x == 0 ? w.q00 : w.q01;
@@ -1279,7 +1217,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       }
-    }
+    } while (false);  // one segment (a `continue` above ends it)
   }
 
   ptx::tc_fence_before();
@@ -1930,8 +1868,8 @@ static int launch_sk(const void* q, const void* k, const void* v, void* o, int h
   if (!sc.one_seg || g_force_path.load() == 2)
     return launch_pk<HD, BF16>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, kv_cap, causal, scale, sp.ws_o, sp.ws_ml, stream, dev,
                                pg, lse);
-  auto kern = fa_prefill_sk_kernel<HD, BF16, true>;
-  if (!sk_attr(kern, dev, (HD == 128 ? 2 : 0) + (BF16 ? 1 : 0) + 4, SL::REQUEST)) return FA_ERR_SMEM;
+  auto kern = fa_prefill_sk_kernel<HD, BF16>;
+  if (!sk_attr(kern, dev, (HD == 128 ? 2 : 0) + (BF16 ? 1 : 0), SL::REQUEST)) return FA_ERR_SMEM;
   std::memcpy(sp.su, sc.su, sizeof(int) * (sc.G + 1));
   std::memcpy(sp.sj, sc.sj, sizeof(int) * (sc.G + 1));
   std::memcpy(sp.pf, sc.pf, sizeof(short) * sc.G);
@@ -2252,8 +2190,8 @@ static int launch_sk_static(const void* q, const void* k, const void* v, void* o
   sp.ws_o = reinterpret_cast<float4*>(base + STATIC_O_OFF);
   if (!sc.one_seg)  // as the workspace path: multi-segment CTAs on the persistent kernel
     return launch_pk<HD, BF16>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, kv_cap, causal, scale, sp.ws_o, sp.ws_ml, stream, dev);
-  auto kern = fa_prefill_sk_kernel<HD, BF16, true>;
-  if (!sk_attr(kern, dev, (HD == 128 ? 2 : 0) + (BF16 ? 1 : 0) + 4, SL::REQUEST)) return FA_ERR_SMEM;
+  auto kern = fa_prefill_sk_kernel<HD, BF16>;
+  if (!sk_attr(kern, dev, (HD == 128 ? 2 : 0) + (BF16 ? 1 : 0), SL::REQUEST)) return FA_ERR_SMEM;
   EncodeTiledFn enc = encoder();
   if (!enc) return FA_ERR_LAUNCH;
   // the maps describe the caller's head width hd (<= HD): TMA zero-fills the
