@@ -6,51 +6,46 @@
 // per-tile steps: minfer "53 · r50 — FA_TKV 32->16 occupancy experiment",
 // section 2): TMA loads into a K/V ring, S = Q K^T and O += P V on the tensor
 // core with accumulators in TMEM, a thread-per-row online softmax with a lazy
-// O rescale.  What is new is how consecutive units follow each other:
+// O rescale.  What is new is how consecutive segments follow each other:
 //
 //   * one K/V ring and one sequence of (V_T, K_T+1) pair barriers run across
-//     unit boundaries, so the next unit's first K tile streams in behind the
-//     current unit's last V tile and the MMA thread waits once per step, in
-//     and between units alike;
-//   * a fourth warpgroup (the epilogue) takes O out of TMEM once a unit is
-//     final -- O / l rounded to 16 bits and stored, or, for a piece of a split
-//     unit, the unnormalised O with its m and l written to the workspace -- so
-//     the softmax warps go straight on to the next unit's first S tile, and the
-//     MMA thread waits for the epilogue only before the next unit's first P V
-//     overwrites that O;
-//   * the next unit's Q is loaded as soon as the current unit's last S MMA has
-//     read its Q (hd 128, one Q buffer pair), or a whole unit ahead (hd 64,
-//     two Q buffer pairs), after an L2 prefetch.
+//     segment boundaries, so the next segment's first K tile streams in
+//     behind the current segment's last V tile and the MMA thread waits once
+//     per step, in and between segments alike;
+//   * the next segment's Q is loaded right after its first K, once the last S
+//     MMA of the segment that used the same buffer pair has read it (hd 128:
+//     one Q buffer pair, loaded during the current segment's last step;
+//     hd 64: two, a whole segment ahead), after an L2 prefetch;
+//   * the softmax warps write a segment's output as soon as its last P V has
+//     completed -- O / l rounded to 16 bits straight to the rows, or, for a
+//     piece of a split unit, the unnormalised O with its m and l to the
+//     workspace -- and go on to the next segment's first S tile, which the
+//     tensor core has computed meanwhile.  (A fourth, epilogue warpgroup was
+//     measured and removed: a 512-thread launch alone cost the step chain
+//     ~5 %, more than the epilogue it took off the softmax warps.)
 //
-//   warps 0-3 / 4-7   softmax of tile A / B (one thread per row == TMEM lane)
-//   warp 8            MMA issuer (one thread)
+//   warps 0-3 / 4-7   softmax and epilogue of tile A / B (one thread per row == TMEM lane)
+//   warp 8            MMA issuer (one thread; at hd 64 the whole warp, one lane issuing)
 //   warp 9            TMA producer (one thread)
 //   warps 10, 11      idle (they complete warpgroup 2)
-//   warps 12-15       epilogue (thread r: row r of tile A, then of tile B)
 //
 // The work list comes in one of two forms.  Whole units (no workspace): CTA c
 // takes units c, 2G-1-c, 2G+c, 4G-1-c, ... of the longest-first order (G CTAs,
 // a snake, so long and short units pair up).  Stream-K ranges (a workspace):
 // CTA c takes the contiguous range of (unit, KV step) work from (su[c], sj[c])
-// to (su[c+1], sj[c+1]) of the same schedule the split-KV path uses, and
-// fa_sk_merge_kernel combines the split units' pieces afterwards.
+// to (su[c+1], sj[c+1]) of the split-KV schedule, and fa_sk_merge_kernel
+// combines the split units' pieces afterwards.
 
 namespace fa {
 
-constexpr int PK_THREADS = 512;
-constexpr int PK_EPI_WARP = 12;  // first epilogue warp
-constexpr uint32_t PK_LAUNCH_REGS = 128;  // 65536 / 512
+constexpr int PK_THREADS = NUM_THREADS;  // softmax A, softmax B, control
 constexpr uint32_t PK_REGS_SOFTMAX = 208;
 constexpr uint32_t PK_REGS_CONTROL = 56;
-constexpr uint32_t PK_REGS_EPI = 40;
-static_assert(256 * PK_REGS_SOFTMAX + 128 * PK_REGS_CONTROL + 128 * PK_REGS_EPI <= PK_THREADS * PK_LAUNCH_REGS,
+static_assert(128 * PK_REGS_CONTROL + 256 * PK_REGS_SOFTMAX <= NUM_THREADS * LAUNCH_REGS,
               "register split exceeds the launch allocation");
 
-// Watchdog codes of this kernel (bits 0-7 of g_fa_status), beside the shared ones.
+// Watchdog code of this kernel (bits 0-7 of g_fa_status), beside the shared ones.
 enum : uint32_t {
-  WD_EPI_O_FULL = 14,
-  WD_MMA_O_EMPTY = 15,
-  WD_SOFTMAX_ML_EMPTY = 16,
   WD_SMEM_ALIGN = 17,  // the dynamic shared memory base is not 1024-byte aligned: nothing was run
 };
 
@@ -64,11 +59,9 @@ struct PkLayout {
   static constexpr uint32_t QSET = 2 * L::Q_BYTES;  // Q_A, Q_B
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_RING = NQB * QSET;
-  static constexpr uint32_t OFF_ML = OFF_RING + NSLOT * L::SLOT_BYTES;  // f32 [tile][m, l][BM]
-  static constexpr uint32_t OFF_BAR = OFF_ML + 2 * 2 * BM * 4;
-  // q_full[NQB], q_empty[NQB], pair[NPB], empty[NSLOT], s_full[2], p_full[2],
-  // o_full[2], o_empty[2], ml_full[2], ml_empty[2], drain
-  static constexpr uint32_t NUM_BARS = 2 * NQB + NPB + NSLOT + 12 + 1;
+  static constexpr uint32_t OFF_BAR = OFF_RING + NSLOT * L::SLOT_BYTES;
+  // q_full[NQB], q_empty[NQB], pair[NPB], empty[NSLOT], s_full[2], p_full[2], o_full[2], drain
+  static constexpr uint32_t NUM_BARS = 2 * NQB + NPB + NSLOT + 6 + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
   static constexpr uint32_t BYTES = OFF_MISC + 16;
   // The kernel declares its dynamic shared memory 1024-byte aligned (the
@@ -133,7 +126,6 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
   }
   const uint32_t sQ = sbase + PL::OFF_Q;
   const uint32_t sRing = sbase + PL::OFF_RING;
-  float* ml = reinterpret_cast<float*>(pk_smem + PL::OFF_ML);
   const uint32_t bar = sbase + PL::OFF_BAR;
   auto bQfull = [&](int b) { return bar + 8u * b; };
   auto bQempty = [&](int b) { return bar + 8u * (NQB + b); };
@@ -143,10 +135,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
   auto bSfull = [&](int x) { return bar + 8u * (B0 + x); };
   auto bPfull = [&](int x) { return bar + 8u * (B0 + 2 + x); };
   auto bOfull = [&](int x) { return bar + 8u * (B0 + 4 + x); };
-  auto bOempty = [&](int x) { return bar + 8u * (B0 + 6 + x); };
-  auto bMlFull = [&](int x) { return bar + 8u * (B0 + 8 + x); };
-  auto bMlEmpty = [&](int x) { return bar + 8u * (B0 + 10 + x); };
-  const uint32_t bDrain = bar + 8u * (B0 + 12);
+  const uint32_t bDrain = bar + 8u * (B0 + 6);
   uint32_t* misc = reinterpret_cast<uint32_t*>(pk_smem + PL::OFF_MISC);
   volatile uint32_t* abort_flag = misc + 1;
 
@@ -165,9 +154,6 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
       ptx::mbar_init(bSfull(x), 1);
       ptx::mbar_init(bPfull(x), BM);   // every softmax thread of the tile
       ptx::mbar_init(bOfull(x), 1);
-      ptx::mbar_init(bOempty(x), 4);   // one per epilogue warp
-      ptx::mbar_init(bMlFull(x), BM);  // every softmax thread of the tile
-      ptx::mbar_init(bMlEmpty(x), BM); // every epilogue thread
     }
     ptx::mbar_init(bDrain, 1);
     misc[1] = 0u;
@@ -185,7 +171,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
   ptx::griddep_launch_dependents();
   ptx::griddep_wait();
 
-  if (warp >= MMA_WARP && warp < PK_EPI_WARP) {
+  if (warp >= MMA_WARP) {
     ptx::setmaxnreg_dec<PK_REGS_CONTROL>();
     if (warp == PRODUCER_WARP && lane == 0) {
       // ------------------------------------------------------------ producer
@@ -307,8 +293,8 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
       // ---------------------------------------------------------- MMA issuer
       // Per segment: S_A(T0), S_B(T0) with K_T0, then per step T the one-shot
       // order P V_A(T), S_A(T+1), P V_B(T), S_B(T+1).  The first P V of a tile
-      // in a segment overwrites its O: it waits until the epilogue has read
-      // the previous segment's O of that tile out of TMEM.
+      // in a segment overwrites its O; it waits for that tile's first P, which
+      // the softmax writes only after it has read the previous segment's O.
       constexpr uint32_t IDESC_S = ptx::idesc_f16(BF16, BM, BN, false, false);  // Q, K both K-major
       constexpr uint32_t IDESC_O = ptx::idesc_f16(BF16, BM, HD, false, true);   // P from TMEM, V MN-major
       constexpr uint32_t DHI = ptx::sdesc_sw128_hi(1024);
@@ -334,7 +320,6 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
       };
       int T = 0;               // KV steps issued over the CTA's segments
       int pc0 = 0, pc1 = 0;    // tiles of A / B so far (s_full / p_full phases)
-      int oc0 = 0, oc1 = 0;    // segments with tiles of A / B so far (o_full commits, o_empty phases)
       int nq = 0;
       bool ok = true;
       int u = 0, jb = 0, je = 0;
@@ -367,11 +352,6 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
             if (t < nXs) {
               ok = mma_wait<CONV>(bPfull(x), ((x == 0 ? pc0 : pc1) + t) & 1, abort_flag, p.watchdog_ns, WD_MMA_P_FULL);
               if (!ok) break;
-              const int oc = x == 0 ? oc0 : oc1;
-              if (t == 0 && oc > 0) {
-                ok = mma_wait<CONV>(bOempty(x), (oc - 1) & 1, abort_flag, p.watchdog_ns, WD_MMA_O_EMPTY);
-                if (!ok) break;
-              }
               ptx::tc_fence_after();
               issue_pv(x, sv, t > 0);
             }
@@ -390,14 +370,8 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
           if (t + 2 == nseg && leader) ptx::mma_commit(bQempty(qb));  // the segment's last S MMAs are issued
         }
         if (!ok) break;
-        if (nAs > 0) {
-          if (leader) ptx::mma_commit(bOfull(0));
-          ++oc0;
-        }
-        if (nBs > 0) {
-          if (leader) ptx::mma_commit(bOfull(1));
-          ++oc1;
-        }
+        if (nAs > 0 && leader) ptx::mma_commit(bOfull(0));
+        if (nBs > 0 && leader) ptx::mma_commit(bOfull(1));
         pc0 += nAs;
         pc1 += nBs;
         ++nq;
@@ -405,101 +379,6 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
       // every MMA issued has finished before TMEM is freed
       if (leader) ptx::mma_commit(bDrain);
       drain_wait(bDrain, 0, DRAIN_NS);
-    }
-  } else if (warp >= PK_EPI_WARP) {
-    ptx::setmaxnreg_dec<PK_REGS_EPI>();
-    // -------------------------------------------------------------- epilogue
-    const int q = warp - PK_EPI_WARP;  // TMEM lane quarter
-    const int r = q * 32 + lane;       // row in the tile
-    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    int oc0 = 0, oc1 = 0;
-    bool ok = true;
-    int u = 0, jb = 0, je = 0;
-    UnitGeo w{};
-    for (int k = 0; ok && pk_segment(sp, cta, k, u, jb, je, w); ++k) {
-      const bool whole = jb == 0 && je >= w.n;
-#pragma unroll 1
-      for (int x = 0; x < 2; ++x) {
-        if (x == 1 && !w.has1) continue;
-        const int nX = x == 0 ? w.nA : w.nB;
-        const int ntX = max(0, min(je, nX) - jb);
-        const int q0 = x == 0 ? w.q00 : w.q01;
-        const int hq = x == 0 ? w.hq0 : w.hq1;
-        const uint32_t tO = tmem + lane_off + L::TM_O + x * HD;
-        float m = -INFINITY, l = 0.f;
-        if (ntX > 0) {
-          const int oc = x == 0 ? oc0 : oc1;
-          ok = warp_wait_bar(bOfull(x), oc & 1, abort_flag, p.watchdog_ns, WD_EPI_O_FULL);
-          if (ok) ok = warp_wait_bar(bMlFull(x), oc & 1, abort_flag, p.watchdog_ns, WD_EPI_O_FULL);
-          if (!ok) break;
-          ptx::tc_fence_after();
-          m = ml[(x * 2 + 0) * BM + r];
-          l = ml[(x * 2 + 1) * BM + r];
-          ptx::mbar_arrive(bMlEmpty(x));
-        }
-        if (whole) {
-          const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-          if (p.lse && q0 + r < p.Sq) p.lse[(static_cast<size_t>(w.b) * p.Hq + hq) * p.Sq + q0 + r] = row_lse(m, l);
-          uint16_t* orow = p.o + ((static_cast<size_t>(w.b) * p.Sq + q0 + r) * p.Hq + hq) * p.hd;
-          const bool in_rows = q0 + r < p.Sq;
-          const bool a32 = (reinterpret_cast<uintptr_t>(orow) & 31u) == 0;
-#pragma unroll 1
-          for (int c = 0; c < HD / 16; ++c) {  // 16 columns per TMEM load
-            uint32_t v[16];
-            if (ntX > 0) {
-              ptx::tmem_ld16(tO + c * 16, v);
-              ptx::tmem_wait_ld();
-              ptx::reg_fence(v);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 16; ++e) v[e] = 0u;
-            }
-            if (in_rows && 16 * c < p.hd) {
-              uint32_t pk[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e)
-                pk[e] = pack2<BF16>(__uint_as_float(v[2 * e]) * inv_l, __uint_as_float(v[2 * e + 1]) * inv_l);
-              if (a32 && 16 * c + 16 <= p.hd) {
-                ptx::st_global_v8(orow + 16 * c, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
-              } else {
-                *reinterpret_cast<uint4*>(orow + 16 * c) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                if (16 * c + 8 < p.hd) *reinterpret_cast<uint4*>(orow + 16 * c + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-              }
-            }
-          }
-        } else {
-          // a piece of a split unit: (O, m, l) to its workspace slot; the merge kernel writes the output
-          const int ps = jb == 0 ? sp.ph[cta] : sp.pf[cta];
-          if (ps < 0) {
-            if (lane == 0) atomicCAS(&g_fa_status, 0u, WD_PIECE_SLOT | ((blockIdx.x < 0xFFFFFFu ? blockIdx.x : 0xFFFFFFu) << 8));
-          } else {
-            const size_t slot_t = static_cast<size_t>(ps) * 2 + x;
-            if (ntX > 0) {
-              float4* dst = sp.ws_o + slot_t * (HD / 4) * BM + r;
-#pragma unroll 1
-              for (int c = 0; c < HD / 16; ++c) {
-                uint32_t v[16];
-                ptx::tmem_ld16(tO + c * 16, v);
-                ptx::tmem_wait_ld();
-                ptx::reg_fence(v);
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                  dst[(c * 4 + e) * BM] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
-                                                      __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
-              }
-            }
-            sp.ws_ml[(slot_t * 2 + 0) * BM + r] = m;
-            sp.ws_ml[(slot_t * 2 + 1) * BM + r] = l;
-          }
-        }
-        if (ntX > 0) {  // every TMEM load of O_X has completed: the next segment's P V may overwrite it
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(bOempty(x));
-          if (x == 0) ++oc0;
-          else ++oc1;
-        }
-      }
     }
   } else {
     ptx::setmaxnreg_inc<PK_REGS_SOFTMAX>();
@@ -512,7 +391,31 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
     const int off = p.Skv - p.Sq;
     const float sl2 = p.sl2;
     int cnt = 0;   // tiles processed (s_full / p_full phases)
-    int mcnt = 0;  // segments with tiles of x (ml hand-offs)
+    int ocnt = 0;  // segments with tiles of x (o_full phases)
+    // O / l of row r rounded to 16 bits, straight to the output row (32-byte
+    // stores where the row is 32-byte aligned), up to the head's true width;
+    // and the row's log-sum-exp when asked for
+    auto store_row = [&](int q0, int hq, int b, float m, float l, const uint32_t (&orr)[HD]) {
+      if (q0 + r >= p.Sq) return;
+      if (p.lse) p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.Sq + q0 + r] = row_lse(m, l);
+      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      uint16_t* orow = p.o + ((static_cast<size_t>(b) * p.Sq + q0 + r) * p.Hq + hq) * p.hd;
+      const bool a32 = (reinterpret_cast<uintptr_t>(orow) & 31u) == 0;
+#pragma unroll
+      for (int c = 0; c < HD / 16; ++c) {
+        if (16 * c >= p.hd) break;
+        uint32_t pk[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          pk[e] = pack2<BF16>(__uint_as_float(orr[16 * c + 2 * e]) * inv_l, __uint_as_float(orr[16 * c + 2 * e + 1]) * inv_l);
+        if (a32 && 16 * c + 16 <= p.hd) {
+          ptx::st_global_v8(orow + 16 * c, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
+        } else {
+          *reinterpret_cast<uint4*>(orow + 16 * c) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          if (16 * c + 8 < p.hd) *reinterpret_cast<uint4*>(orow + 16 * c + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+      }
+    };
     bool ok = true;
     int u = 0, jb = 0, je = 0;
     UnitGeo w{};
@@ -520,7 +423,24 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
       const int q0 = x == 0 ? w.q00 : w.q01;
       const int nX = x == 0 ? w.nA : w.nB;
       const int jx_end = min(je, nX);
-      if (jx_end <= jb) continue;  // no tile of x in this segment (the epilogue knows)
+      const int hqx = x == 0 ? w.hq0 : w.hq1;
+      if (jx_end <= jb) {  // no KV tile of x in this segment
+        if (x == 1 && !w.has1) continue;
+        if (jb == 0 && je >= w.n) {  // a whole unit whose rows see no key: O = 0
+          uint32_t orr[HD];
+#pragma unroll
+          for (int e = 0; e < HD; ++e) orr[e] = 0u;
+          store_row(q0, hqx, w.b, -INFINITY, 0.f, orr);
+        } else {
+          const int ps = jb == 0 ? sp.ph[cta] : sp.pf[cta];
+          if (ps >= 0) {
+            const size_t slot_t = static_cast<size_t>(ps) * 2 + x;
+            sp.ws_ml[(slot_t * 2 + 0) * BM + r] = -INFINITY;
+            sp.ws_ml[(slot_t * 2 + 1) * BM + r] = 0.f;
+          }
+        }
+        continue;
+      }
       const int kv_all = p.causal ? min(p.Skv, off + q0 + 1) : p.Skv;       // keys every row sees
       const int row_lim = p.causal ? min(p.Skv, off + q0 + r + 1) : p.Skv;  // keys this row sees
       float m_ref = -INFINITY;  // running max (log2 domain) that O and l are scaled to
@@ -607,17 +527,39 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
         ptx::mbar_arrive(bPfull(x));
       }
       if (!ok) break;
-      // the segment's (m, l) to the epilogue, once it has read the previous ones
-      if (mcnt > 0) {
-        ok = warp_wait_bar(bMlEmpty(x), (mcnt - 1) & 1, abort_flag, p.watchdog_ns, WD_SOFTMAX_ML_EMPTY);
-        if (!ok) break;
+      // ------------------------------------------------------------ epilogue
+      // O_X of this segment is final once its last P V has completed; it is
+      // read out before this thread writes the next segment's first P, which
+      // is what lets the MMA thread overwrite O_X.
+      ok = warp_wait_bar(bOfull(x), ocnt & 1, abort_flag, p.watchdog_ns, WD_SOFTMAX_O_DONE);
+      if (!ok) break;
+      ++ocnt;
+      ptx::tc_fence_after();
+      uint32_t orr[HD];  // the whole row: all loads in flight before one wait
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) ptx::tmem_ld32(tO + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&orr[c * 32]));
+      ptx::tmem_wait_ld();
+      ptx::reg_fence(orr);
+      if (jb == 0 && je >= w.n) {  // a whole unit: O / l to the row
+        store_row(q0, hqx, w.b, m_ref, l, orr);
+      } else {  // a piece of a split unit: (O, m, l) to its workspace slot
+        const int ps = jb == 0 ? sp.ph[cta] : sp.pf[cta];
+        if (ps < 0) {
+          if (lane == 0) atomicCAS(&g_fa_status, 0u, WD_PIECE_SLOT | ((blockIdx.x < 0xFFFFFFu ? blockIdx.x : 0xFFFFFFu) << 8));
+          continue;
+        }
+        const size_t slot_t = static_cast<size_t>(ps) * 2 + x;
+        float4* dst = sp.ws_o + slot_t * (HD / 4) * BM + r;
+#pragma unroll
+        for (int e = 0; e < HD / 4; ++e)
+          dst[e * BM] = make_float4(__uint_as_float(orr[4 * e]), __uint_as_float(orr[4 * e + 1]),
+                                    __uint_as_float(orr[4 * e + 2]), __uint_as_float(orr[4 * e + 3]));
+        sp.ws_ml[(slot_t * 2 + 0) * BM + r] = m_ref;
+        sp.ws_ml[(slot_t * 2 + 1) * BM + r] = l;
       }
-      ml[(x * 2 + 0) * BM + r] = m_ref;
-      ml[(x * 2 + 1) * BM + r] = l;
-      ptx::mbar_arrive(bMlFull(x));
-      ++mcnt;
     }
   }
+
 
   // ---- teardown: every role is done (or has drained); free TMEM
   ptx::tc_fence_before();
