@@ -342,7 +342,7 @@ def run_ours(args):
         copies.append((q.to(dev), k.to(dev), v.to(dev), torch.empty_like(q, device=dev)))
     stream = torch.cuda.current_stream(dev)
     split = (args.path == "split" or
-             (args.path == "auto" and fa.split_kv_advised(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.causal)))
+             (args.path == "auto" and fa.split_kv_advised(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.causal, w.hd)))
     paged = args.page_size > 0
     if paged:  # each copy's K/V scattered over a pool in shuffled page order
         page = args.page_size

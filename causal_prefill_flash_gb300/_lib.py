@@ -34,6 +34,7 @@ _SIG = {
                                 _P]),
     "fa_workspace_bytes": (ctypes.c_size_t, [_I]),
     "fa_split_kv_advised": (_I, [_I, _I, _I, _I, _I, _I]),
+    "fa_split_kv_advised_hd": (_I, [_I, _I, _I, _I, _I, _I, _I]),
     "fa_prefill_ex": (_I, [_P, _P, _P, _P, _P] + [_I] * 7 + [ctypes.c_float, _I, _P, ctypes.c_size_t, _P]),
     "fa_prefill_kvcache": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _I, _P,
                                 ctypes.c_size_t, _P]),
@@ -240,7 +241,7 @@ def attention_paged(q, k_pool, v_pool, block_table, kv_len: int, causal: bool = 
     elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
         raise ValueError("out must be a contiguous CUDA tensor like q")
     if split is None:
-        split = hd <= 128 and split_kv_advised(B, Hq, Hkv, Sq, kv_len, causal)
+        split = hd <= 128 and split_kv_advised(B, Hq, Hkv, Sq, kv_len, causal, hd)
     if split:
         ws = workspace_for(q.device, hd, stream)
         st = fa_prefill_paged_ws(q, k_pool, v_pool, block_table, out, B, Hq, Hkv, Sq, kv_len, hd, page_size,
@@ -309,7 +310,7 @@ def attention_kvcache(q, k_cache, v_cache, kv_len: int, causal: bool = True, sca
     elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
         raise ValueError("out must be a contiguous CUDA tensor like q")
     if split is None:
-        split = hd <= 128 and split_kv_advised(B, Hq, Hkv, Sq, kv_len, causal)
+        split = hd <= 128 and split_kv_advised(B, Hq, Hkv, Sq, kv_len, causal, hd)
     ws = workspace_for(q.device, hd, stream) if split else None
     st = fa_prefill_kvcache(q, k_cache, v_cache, out, B, Hq, Hkv, Sq, kv_len, kv_cap, hd, int(bool(causal)),
                             scale, int(q.dtype == torch.bfloat16), ws, ws.numel() if ws is not None else 0, stream)
@@ -326,10 +327,15 @@ def fa_prefill_ex(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, hd, causal, scale, bf16,
                                     _ptr(workspace), int(workspace_bytes), _stream(stream)))
 
 
-def split_kv_advised(B, Hq, Hkv, Sq, Skv, causal=True) -> bool:
+def split_kv_advised(B, Hq, Hkv, Sq, Skv, causal=True, hd=None) -> bool:
     """The library's advice for this shape on the current device: True when the
-    split-KV kernel is expected to beat the one-shot kernel."""
-    st = int(load().fa_split_kv_advised(int(B), int(Hq), int(Hkv), int(Sq), int(Skv), int(bool(causal))))
+    split-KV path is expected to beat the one-shot kernel.  With ``hd`` the
+    head-width-aware rule (fa_split_kv_advised_hd) is used."""
+    if hd is None:
+        st = int(load().fa_split_kv_advised(int(B), int(Hq), int(Hkv), int(Sq), int(Skv), int(bool(causal))))
+    else:
+        st = int(load().fa_split_kv_advised_hd(int(B), int(Hq), int(Hkv), int(Sq), int(Skv), int(hd),
+                                               int(bool(causal))))
     if st < 0:
         raise FaError(-st, "fa_split_kv_advised")
     return st == 1
@@ -388,7 +394,7 @@ def attention(q, k, v, causal: bool = True, scale: float | None = None, out=None
     elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
         raise ValueError("out must be a contiguous CUDA tensor like q")
     if split is None:  # split-KV exists for heads up to 128 wide
-        split = hd <= 128 and split_kv_advised(B, Hq, Hkv, Sq, Skv, causal)
+        split = hd <= 128 and split_kv_advised(B, Hq, Hkv, Sq, Skv, causal, hd)
     if return_lse:
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
         ws = workspace_for(q.device, hd, stream) if split else None

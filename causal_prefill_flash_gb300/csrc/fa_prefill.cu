@@ -2292,17 +2292,65 @@ extern "C" int fa_prefill_ex(const void* q, const void* k, const void* v, void* 
                     stream);
 }
 
-extern "C" int fa_split_kv_advised(int B, int Hq, int Hkv, int Sq, int Skv, int causal) {
-  (void)causal;  // the longest query tile walks all Skv keys either way (bottom-right alignment)
+namespace fa {
+
+// The one-shot grid's wave efficiency: its pairs run longest first in waves
+// of `sms`, so each wave lasts as long as its first (longest) pair; the
+// efficiency is the pairs' KV steps over sms x that sum.  Host-only.
+static double oneshot_wave_efficiency(int B, int Hq, int Hkv, int Sq, int Skv, int causal, int sms) {
+  Params prm;
+  std::memset(&prm, 0, sizeof(prm));
+  prm.B = B;
+  prm.Hq = Hq;
+  prm.Hkv = Hkv;
+  prm.Sq = Sq;
+  prm.Skv = Skv;
+  prm.G = Hq / Hkv;
+  prm.n_qtiles = (Sq + BM - 1) / BM;
+  prm.pair_heads = (prm.G % 2 == 0) ? 1 : 0;
+  prm.causal = causal ? 1 : 0;
+  const long long nu = unit_count_of(prm);
+  long long total = 0, makespan = 0;
+  for (long long u = 0; u < nu; ++u) {
+    const int n = unit_geo(prm, static_cast<int>(u)).n;
+    total += n;
+    if (u % sms == 0) makespan += n;
+  }
+  return makespan > 0 ? static_cast<double>(total) / (static_cast<double>(sms) * makespan) : 1.0;
+}
+
+static int split_advice(int B, int Hq, int Hkv, int Sq, int Skv, int hd, int causal) {
   if (B < 0 || Sq < 0 || Skv < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return -FA_ERR_INVALID_ARG;
+  if (hd != 0 && kernel_hd(hd) == 0) return -FA_ERR_UNSUPPORTED;
   if (B == 0 || Sq == 0 || Skv == 0) return 0;
+  if (hd > 128) return 0;  // split-KV takes heads up to 128 wide
   int dev = -1;
-  const int ds = fa::check_device(&dev);
+  const int ds = check_device(&dev);
   if (ds != FA_OK) return -ds;
-  const long long units = fa::grid_size(B, Hq, Hkv, Sq);
-  const long long longest = (Skv + fa::BN - 1) / fa::BN;
-  const long long sms = fa::g_dev_sms[dev].load();
-  return (2 * units <= sms && longest >= 8) ? 1 : 0;
+  const long long units = grid_size(B, Hq, Hkv, Sq);
+  const long long longest = (Skv + BN - 1) / BN;
+  const long long sms = g_dev_sms[dev].load();
+  // an underfilled one-shot grid with long rows (causal or not, the longest
+  // query tile walks all Skv keys under the bottom-right alignment)
+  if (2 * units <= sms && longest >= 8) return 1;
+  // hd 64: more pairs than SMs, but whole waves of them leave SMs idle --
+  // the persistent kernel's stream-K ranges even the load out, and at hd 64
+  // it steps as fast as the one-shot kernel (at hd 128 it is 10-15 % slower
+  // per step, more than the quantization it removes)
+  if (hd != 0 && kernel_hd(hd) == 64 && units > sms && units <= (1 << 20) &&
+      oneshot_wave_efficiency(B, Hq, Hkv, Sq, Skv, causal, static_cast<int>(sms)) < 0.88)
+    return 1;
+  return 0;
+}
+
+}  // namespace fa
+
+extern "C" int fa_split_kv_advised(int B, int Hq, int Hkv, int Sq, int Skv, int causal) {
+  return fa::split_advice(B, Hq, Hkv, Sq, Skv, 0, causal);
+}
+
+extern "C" int fa_split_kv_advised_hd(int B, int Hq, int Hkv, int Sq, int Skv, int hd, int causal) {
+  return fa::split_advice(B, Hq, Hkv, Sq, Skv, hd, causal);
 }
 
 extern "C" int fa_prefill_ws_static(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,

@@ -70,7 +70,7 @@
  *   fa_prefill, fa_prefill_bf16      one-shot kernel (hd 8 .. 256, multiples of 8)
  *   fa_prefill_ws, fa_prefill_ws_bf16  split-KV kernel with a caller workspace
  *   fa_workspace_bytes               its workspace size
- *   fa_split_kv_advised              which of the two kernels to use for a shape
+ *   fa_split_kv_advised(_hd)         whether to take split-KV for a shape
  *   fa_prefill_ex                    either kernel, any hd, optional log-sum-exp
  *   fa_prefill_kvcache               attention over a K/V cache of capacity kv_cap
  *   fa_prefill_paged, fa_prefill_paged_ws  attention over a paged K/V pool
@@ -213,6 +213,22 @@ int fa_prefill_ex(const void* q, const void* k, const void* v, void* o,
  * count once (cached); launches nothing.
  */
 int fa_split_kv_advised(int B, int Hq, int Hkv, int Sq, int Skv, int causal);
+
+/*
+ * fa_split_kv_advised_hd -- fa_split_kv_advised for a known head width hd
+ * (the same returns; -FA_ERR_UNSUPPORTED for an hd no kernel takes; 0 for hd
+ * over 128, which split-KV does not take).  Besides the underfilled-grid rule
+ * above it advises split-KV for heads up to 64 wide when there are more
+ * query-tile pairs than SMs but the one-shot grid's waves leave SMs idle: the
+ * pairs run longest first in waves of one per SM, each wave as long as its
+ * longest pair, and when the pairs' KV steps fill less than 88 % of
+ * SMs x that time, the split-KV schedule's equal stream-K ranges (run by the
+ * persistent kernel) finish sooner.  That is the page's split-K rule again --
+ * split when the tiles cannot cover the part evenly -- for a grid of a few
+ * more pairs than SMs (e.g. the chunked prefill, 256 pairs of ~63 KV steps on
+ * 152 SMs).  Host-only; launches nothing.
+ */
+int fa_split_kv_advised_hd(int B, int Hq, int Hkv, int Sq, int Skv, int hd, int causal);
 
 /*
  * fa_prefill_kvcache -- attention over a K/V cache, the read side of a

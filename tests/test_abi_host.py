@@ -146,6 +146,11 @@ def test_split_advice_rejects_bad_sizes_without_a_device(fa):
     assert f(-1, 4, 2, 8, 8, 1) == -1
     assert f(0, 4, 2, 8, 8, 1) == 0       # nothing to compute: no advice needed, no device touched
     assert f(1, 4, 2, 8, 0, 1) == 0
+    g = fa._lib.load().fa_split_kv_advised_hd
+    assert g(1, 3, 2, 8, 8, 64, 1) == -1     # Hq % Hkv != 0
+    assert g(1, 4, 2, 8, 8, 100, 1) == -2    # no kernel takes hd 100
+    assert g(0, 4, 2, 8, 8, 64, 1) == 0
+    assert g(1, 4, 2, 8, 8, 256, 1) == 0     # split-KV takes heads up to 128 wide
 
 
 def test_kvcache_and_append_errors_without_a_device(fa):

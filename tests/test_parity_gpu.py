@@ -284,16 +284,21 @@ def test_workload_full_size_sampled_rows(idx, split):
 
 
 def test_split_advice_follows_the_grid_fill():
-    """The library advises split-KV only where the one-shot grid leaves most SMs
-    idle and rows are long: the long-context chunk, not the square prompts."""
+    """The library advises split-KV where the one-shot grid leaves most SMs
+    idle and rows are long (the long-context chunk), and -- knowing the head
+    width -- for hd 64 grids of a few more pairs than SMs whose waves leave SMs
+    idle (the chunked hd 64 prefill: 256 pairs on 152 SMs); not for the square
+    prompts, not at hd 128 or 256."""
     fa = _fa()
     W_ = {w.name: w for w in W.WORKLOADS}
     adv = lambda w: fa.split_kv_advised(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.causal)
-    assert adv(W_["longctx_chunk128_kv32768"])
+    adv_hd = lambda w: fa.split_kv_advised(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.causal, w.hd)
+    assert adv(W_["longctx_chunk128_kv32768"]) and adv_hd(W_["longctx_chunk128_kv32768"])
     for name in ("single_head_s256", "prefill7b_s2048", "ragged_s2659_std3", "gqa_s8192_bf16",
                  "chunked_kv8192_hd128", "chunked_kv8192_hd64", "encoder_s4096_noncausal",
                  "gqa_s4096_hd256_bf16"):
         assert not adv(W_[name]), name
+        assert adv_hd(W_[name]) == (name == "chunked_kv8192_hd64"), name
 
 
 # ------------------------------------------------------ many-CTA / sparse grids
