@@ -88,6 +88,18 @@ def job_throughput(flops_per_step_per_rank: int, world: int, ms_per_step: float)
     return flops_per_step_per_rank * world / (ms_per_step * 1e-3) / 1e12
 
 
+def split_kernel_label(fa, w):
+    """Which kernels the split-KV path runs for the workload: one piece per CTA
+    on the split-KV kernel, several segments per CTA on the persistent kernel;
+    the merge kernel after either when pairs are split."""
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    sc = fa.debug_schedule(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.causal, sms=sms)
+    k = "fa_prefill_sk_kernel (split-KV, one piece per CTA)" if sc["one_segment"] else \
+        "fa_prefill_pk_kernel (persistent, stream-K ranges)"
+    return k + (" + fa_sk_merge_kernel" if sc["split_pairs"] else "")
+
+
 def burst_spread(per_burst):
     """Median, 10th and 90th percentile (nearest rank) and extremes of the
     per-burst ms/step figures."""
@@ -510,7 +522,7 @@ def run_ours(args):
                    "flops_per_call": flops, "flop_convention": "4*hd*visible (query,key) pairs",
                    "l2": f"inputs rotated over {ncopy} resident copies ({ncopy * io / 1e6:.0f} MB > L2)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "kernel": "fa_prefill_sk_kernel (split-KV)" if split else "fa_prefill_kernel (one-shot)",
+                   "kernel": split_kernel_label(fa, w) if split else "fa_prefill_kernel (one-shot)",
                    "kv_layout": f"paged, {args.page_size}-token pages in shuffled order" if paged
                    else "contiguous BSHD"},
         "pct_of_peak": 100.0 * achieved / peak,
@@ -523,7 +535,8 @@ def run_ours(args):
         "clocks": clocks.summary(),
         "e2e": e2e,
         "cpu_baseline": cpu,
-        "gpu_launches": args.steps * (2 if split else 1),  # split-KV: the stream-K kernel and the merge
+        "gpu_launches": args.steps * (2 if split and "merge" in split_kernel_label(fa, w) else 1),
+        # split-KV: the attention kernel, and the merge when pairs are split
         "watchdog_status": watchdog,
     }
     print(json.dumps(line), flush=True)
