@@ -100,6 +100,28 @@ def split_kernel_label(fa, w):
     return k + (" + fa_sk_merge_kernel" if sc["split_pairs"] else "")
 
 
+CLOCK_WINDOW_S = 1.0  # the clock record covers at least this much load
+
+
+def keep_loaded(step, first, t_start):
+    """When the warm-up and timed steps together last less than the clock
+    sampler's window, keep running the same steps (untimed, after the timed
+    region) until they do, so that the clock record samples the GPU under this
+    load; returns a description of the sampled window."""
+    import torch
+    i = first
+    extra = 0
+    while time.time() - t_start < CLOCK_WINDOW_S:
+        for _ in range(16):
+            step(i)
+            i += 1
+            extra += 1
+        torch.cuda.synchronize()
+    if extra == 0:
+        return "warm-up and timed steps"
+    return f"warm-up and timed steps, then {extra} more of the same steps after the timed region (untimed)"
+
+
 def burst_spread(per_burst):
     """Median, 10th and 90th percentile (nearest rank) and extremes of the
     per-burst ms/step figures."""
@@ -425,6 +447,7 @@ def run_ours(args):
                 i += 1
             ev[b + 1].record(stream)
         torch.cuda.synchronize()
+        load_window = keep_loaded(step, args.steps, t_load0)
         clocks.mark(t_load0, time.time())
         barrier()
         torch.cuda.synchronize()
@@ -532,7 +555,7 @@ def run_ours(args):
                      "traffic": traffic,
                      "algorithmic_bytes": io,
                      "achieved_hbm_gbs": io / (ms_step * 1e-3) / 1e9},
-        "clocks": clocks.summary(),
+        "clocks": dict(clocks.summary(), window=load_window),
         "e2e": e2e,
         "cpu_baseline": cpu,
         "gpu_launches": args.steps * (2 if split and "merge" in split_kernel_label(fa, w) else 1),
@@ -597,6 +620,7 @@ def run_append(args):
             step(i)
         e1.record(stream)
         torch.cuda.synchronize()
+        load_window = keep_loaded(step, args.steps, t0)
         clocks.mark(t0, time.time())
     ms = e0.elapsed_time(e1) / args.steps
     gbs = step_bytes / (ms * 1e-3) / 1e9
@@ -611,7 +635,8 @@ def run_append(args):
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                      "peak_source": f"{peak_src} copy bandwidth",
                      "traffic": recorded_traffic(w.name + ":append")},
-        "clocks": clocks.summary(), "gpu_launches": args.steps, "watchdog_status": fa.debug_status(),
+        "clocks": dict(clocks.summary(), window=load_window), "gpu_launches": args.steps,
+        "watchdog_status": fa.debug_status(),
     }
     print(json.dumps(line), flush=True)
     return 0
