@@ -20,3 +20,16 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture
+def force_persistent():
+    """Run the test's split-KV calls on the persistent kernel, whatever their
+    schedule (the library otherwise runs one-piece-per-CTA schedules on the
+    split-KV kernel); the library's own choice is restored afterwards."""
+    import causal_prefill_flash_gb300 as fa
+    fa.debug_force_path("persistent")
+    try:
+        yield
+    finally:
+        fa.debug_force_path("auto")

@@ -34,13 +34,16 @@ def _check(got, want, dtype, what):
     assert not bad.any(), f"{what}: {int(bad.sum())} of {err.size} out of tolerance, max err {np.nanmax(err):.3e}"
 
 
-@pytest.mark.parametrize("split", [False, True], ids=["oneshot", "streamk"])
+@pytest.mark.parametrize("split", [False, True, "persistent"], ids=["oneshot", "splitkv", "persistent"])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-def test_output_feeds_the_next_call(dtype, split):
+def test_output_feeds_the_next_call(dtype, split, request):
     """O1 = attn(Q, K, V); O2 = attn(O1, K, V); O3 = attn(Q, O2, V): the
     second call reads the first's output as its queries, the third the
     second's output as its keys."""
     fa = _fa()
+    if split == "persistent":  # the split-KV schedule on the persistent kernel
+        request.getfixturevalue("force_persistent")
+        split = True
     B, H, S, hd = 1, 8, 700, 128
     w = W.Workload("chain", B, H, H, S, S, hd, dtype=dtype, seed=11)
     q, k, v = (t.cuda() for t in W.make_inputs(w))

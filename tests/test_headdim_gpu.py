@@ -109,9 +109,14 @@ def test_head_width_paged_and_cache():
             n = min(kv_len, (p + 1) * page) - p * page
             kp[perm[b, p], :n] = k[b, p * page: p * page + n]
             vp[perm[b, p], :n] = v[b, p * page: p * page + n]
-    for split in (False, True):
-        out = fa.attention_paged(q.cuda(), kp.cuda(), vp.cuda(), perm.cuda(), kv_len, causal=True, scale=w.scale,
-                                 split=split)
+    for split in (False, True, "persistent"):
+        if split == "persistent":
+            fa.debug_force_path("persistent")
+        try:
+            out = fa.attention_paged(q.cuda(), kp.cuda(), vp.cuda(), perm.cuda(), kv_len, causal=True, scale=w.scale,
+                                     split=bool(split))
+        finally:
+            fa.debug_force_path("auto")
         torch.cuda.synchronize()
         assert fa.debug_status() == 0
         _check(out.cpu(), want, "f16", f"paged split{split}")
@@ -120,8 +125,14 @@ def test_head_width_paged_and_cache():
     vc = torch.full_like(kc, float("nan"))
     kc[:, :kv_len] = k
     vc[:, :kv_len] = v
-    for split in (False, True):
-        out = fa.attention_kvcache(q.cuda(), kc.cuda(), vc.cuda(), kv_len, causal=True, scale=w.scale, split=split)
+    for split in (False, True, "persistent"):
+        if split == "persistent":
+            fa.debug_force_path("persistent")
+        try:
+            out = fa.attention_kvcache(q.cuda(), kc.cuda(), vc.cuda(), kv_len, causal=True, scale=w.scale,
+                                       split=bool(split))
+        finally:
+            fa.debug_force_path("auto")
         torch.cuda.synchronize()
         assert fa.debug_status() == 0
         _check(out.cpu(), want, "f16", f"cache split{split}")

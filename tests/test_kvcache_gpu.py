@@ -92,9 +92,15 @@ def test_kv_append_skips_and_reports_out_of_range_positions():
     assert np.array_equal(_bits(kc), wk) and np.array_equal(_bits(vc), wv)
 
 
-@pytest.fixture(params=[False, True], ids=["oneshot", "streamk"])
+@pytest.fixture(params=[False, True, "persistent"], ids=["oneshot", "splitkv", "persistent"])
 def split(request):
-    return request.param
+    """The one-shot kernel; the split-KV path as the library routes it; and the
+    split-KV schedule forced onto the persistent kernel."""
+    if request.param != "persistent":
+        yield request.param
+        return
+    request.getfixturevalue("force_persistent")
+    yield True
 
 
 @pytest.mark.parametrize("bf16", [False, True], ids=["f16", "bf16"])

@@ -29,7 +29,7 @@ def _check_lse(got, want):
     assert err.size == 0 or err.max() <= 2e-4, err.max()
 
 
-@pytest.mark.parametrize("split", [False, True], ids=["oneshot", "streamk"])
+@pytest.mark.parametrize("split", [False, True, "persistent"], ids=["oneshot", "splitkv", "persistent"])
 @pytest.mark.parametrize("B,Hq,Hkv,Sq,Skv,hd,dtype,causal", [
     (1, 4, 2, 300, 300, 128, "f16", True),
     (2, 3, 1, 129, 1000, 64, "bf16", True),
@@ -37,10 +37,13 @@ def _check_lse(got, want):
     (1, 4, 4, 200, 700, 128, "bf16", False),
     (1, 2, 1, 260, 260, 256, "bf16", True),
 ])
-def test_lse_matches_oracle(B, Hq, Hkv, Sq, Skv, hd, dtype, causal, split):
+def test_lse_matches_oracle(B, Hq, Hkv, Sq, Skv, hd, dtype, causal, split, request):
     fa = _fa()
     if split and hd == 256:
         pytest.skip("split-KV takes hd 64 and 128")
+    if split == "persistent":  # the split-KV schedule on the persistent kernel
+        request.getfixturevalue("force_persistent")
+        split = True
     w = W.Workload("lse", B, Hq, Hkv, Sq, Skv, hd, causal=causal, dtype=dtype, seed=Sq + Skv + hd)
     q, k, v = W.make_inputs(w)
     out, lse = fa.attention(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=w.scale, split=split,

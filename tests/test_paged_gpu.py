@@ -51,9 +51,15 @@ CASES = [  # (B, Hq, Hkv, Sq, kv_len, hd, dtype, page)
 ]
 
 
-@pytest.fixture(params=[False, True], ids=["oneshot", "streamk"])
+@pytest.fixture(params=[False, True, "persistent"], ids=["oneshot", "splitkv", "persistent"])
 def split(request):
-    return request.param
+    """The one-shot kernel; the split-KV path as the library routes it; and the
+    split-KV schedule forced onto the persistent kernel."""
+    if request.param != "persistent":
+        yield request.param
+        return
+    request.getfixturevalue("force_persistent")
+    yield True
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "B{}_H{}-{}_Sq{}_kv{}_hd{}_{}_p{}".format(*c))
