@@ -725,6 +725,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }  // namespace fa
 
 #include "fa_prefill256.cuh"
+#include "fa_prefill64.cuh"
 
 namespace fa {
 
@@ -1487,11 +1488,12 @@ template <int HD, bool BF16>
 static int launch(const void* q, const void* k, const void* v, void* o, int hd, int B, int Hq, int Hkv, int Sq, int Skv,
                   int kv_cap, int causal, float scale, cudaStream_t stream, int dev, const Paged* pg = nullptr,
                   float* lse = nullptr) {
-  using L = Layout<HD>;
-  auto kern = fa_prefill_kernel<HD, BF16>;
+  // heads up to 64 wide run on the kernel with S and P in separate TMEM columns
+  constexpr uint32_t REQUEST = HD == 64 ? Layout64::REQUEST : Layout<HD>::REQUEST;
+  auto kern = HD == 64 ? fa_prefill64_kernel<BF16> : fa_prefill_kernel<HD, BF16>;
   const int slot = (HD == 128 ? 2 : 0) + (BF16 ? 1 : 0);
   if (g_attr_set[dev][slot].load() == 0) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::REQUEST) != cudaSuccess) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)REQUEST) != cudaSuccess) {
       (void)cudaGetLastError();
       return FA_ERR_SMEM;
     }
@@ -1519,7 +1521,7 @@ static int launch(const void* q, const void* k, const void* v, void* o, int hd, 
   prm.sl2 = scale * 1.4426950408889634f;
   prm.watchdog_ns = g_watchdog_ns.load();
   const long long grid = grid_size(B, Hq, Hkv, Sq);
-  if (launch_pdl(kern, dim3((unsigned)grid), dim3(NUM_THREADS), L::REQUEST, stream, mq, mk, mv, mo, mkt, mvt, prm) !=
+  if (launch_pdl(kern, dim3((unsigned)grid), dim3(NUM_THREADS), REQUEST, stream, mq, mk, mv, mo, mkt, mvt, prm) !=
       cudaSuccess) {
     (void)cudaGetLastError();
     return FA_ERR_LAUNCH;
@@ -2410,7 +2412,7 @@ extern "C" int fa_debug_schedule(int B, int Hq, int Hkv, int Sq, int Skv, int ca
 extern "C" unsigned int fa_smem_bytes(int hd) {
   if (fa::kernel_hd(hd) == 256) return fa::Layout256::REQUEST;
   if (fa::kernel_hd(hd) == 128) return fa::Layout<128>::REQUEST;
-  if (fa::kernel_hd(hd) == 64) return fa::Layout<64>::REQUEST;
+  if (fa::kernel_hd(hd) == 64) return fa::Layout64::REQUEST;
   return 0u;
 }
 

@@ -47,13 +47,14 @@ def test_status_strings(fa):
 
 def test_smem_request_matches_the_tile_layout(fa):
     """Two query tiles + a ring of K/V slots (5 at hd = 128, 8 at hd = 64) +
-    one mbarrier for Q, a full/empty pair per slot, two each for S ready, P
-    ready, and one each for the final O and the abort drain + 16 B of flags +
-    1 KB alignment slack; within the 227 KB opt-in limit."""
-    for hd, nslot in ((64, 8), (128, 5)):
+    the mbarriers + 16 B of flags + 1 KB alignment slack; within the 227 KB
+    opt-in limit.  hd 128: one for Q, a full/empty pair per slot, two each
+    for S ready and P ready, the final O, the abort drain, two O-staged.
+    hd 64: one for Q, 4 (V, K) pair barriers, 8 slot frees, two each for S
+    ready, S read, P ready and P V done, the final O, the drain, two O-staged."""
+    for hd, nslot, bars in ((64, 8, 1 + 4 + 8 + 2 * 4 + 1 + 1 + 2), (128, 5, 1 + 2 * 5 + 2 + 2 + 2 + 2)):
         q = 128 * hd * 2
         slot = 128 * hd * 2
-        bars = 1 + 2 * nslot + 2 + 2 + 2 + 2  # + o_staged[2]
         want = 2 * q + nslot * slot + bars * 8 + 16 + 1024
         assert fa.smem_bytes(hd) == want
         assert want <= 227 * 1024
