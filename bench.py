@@ -88,6 +88,16 @@ def job_throughput(flops_per_step_per_rank: int, world: int, ms_per_step: float)
     return flops_per_step_per_rank * world / (ms_per_step * 1e-3) / 1e12
 
 
+def oneshot_kernel_label(w):
+    """The one-shot kernel a head width runs on (heads of 8..64, 72..128 and
+    136..256 columns run on the 64-, 128- and 256-column kernels)."""
+    if w.hd <= 64:
+        return "fa_prefill64_kernel (one-shot, S and P apart in TMEM)"
+    if w.hd <= 128:
+        return "fa_prefill_kernel (one-shot)"
+    return "fa_prefill256_kernel (one-shot)"
+
+
 def split_kernel_label(fa, w):
     """Which kernels the split-KV path runs for the workload: one piece per CTA
     on the split-KV kernel, several segments per CTA on the persistent kernel;
@@ -545,7 +555,7 @@ def run_ours(args):
                    "flops_per_call": flops, "flop_convention": "4*hd*visible (query,key) pairs",
                    "l2": f"inputs rotated over {ncopy} resident copies ({ncopy * io / 1e6:.0f} MB > L2)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "kernel": split_kernel_label(fa, w) if split else "fa_prefill_kernel (one-shot)",
+                   "kernel": split_kernel_label(fa, w) if split else oneshot_kernel_label(w),
                    "kv_layout": f"paged, {args.page_size}-token pages in shuffled order" if paged
                    else "contiguous BSHD"},
         "pct_of_peak": 100.0 * achieved / peak,

@@ -16,6 +16,9 @@
 //     MMA of the segment that used the same buffer pair has read it (hd 128:
 //     one Q buffer pair, loaded during the current segment's last step;
 //     hd 64: two, a whole segment ahead), after an L2 prefetch;
+//   * at hd 64, where TMEM has room for P beside S (as in fa_prefill64.cuh),
+//     S_X(T+1) is issued as soon as softmax X has read S_X(T), not after
+//     P V_X(T), so the tile's chain loses the MMA and its hand-offs;
 //   * the softmax warps write a segment's output as soon as its last P V has
 //     completed -- O / l rounded to 16 bits straight to the rows, or, for a
 //     piece of a split unit, the unnormalised O with its m and l to the
@@ -60,8 +63,12 @@ struct PkLayout {
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_RING = NQB * QSET;
   static constexpr uint32_t OFF_BAR = OFF_RING + NSLOT * L::SLOT_BYTES;
-  // q_full[NQB], q_empty[NQB], pair[NPB], empty[NSLOT], s_full[2], p_full[2], o_full[2], drain
-  static constexpr uint32_t NUM_BARS = 2 * NQB + NPB + NSLOT + 6 + 1;
+  // q_full[NQB], q_empty[NQB], pair[NPB], empty[NSLOT], s_full[2], p_full[2], o_full[2], drain,
+  // s_free[2], pv_done[2] (hd 64: S and P in separate TMEM columns)
+  static constexpr uint32_t NUM_BARS = 2 * NQB + NPB + NSLOT + 6 + 1 + 4;
+  // TMEM: S_A | S_B | O_A | O_B, and at hd 64 P_A | P_B in the 128 columns left
+  static constexpr uint32_t TM_P = L::TM_O + 2 * HD;
+  static constexpr bool SPLIT_P = HD == 64;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
   static constexpr uint32_t BYTES = OFF_MISC + 16;
   // The kernel declares its dynamic shared memory 1024-byte aligned (the
@@ -136,6 +143,10 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
   auto bPfull = [&](int x) { return bar + 8u * (B0 + 2 + x); };
   auto bOfull = [&](int x) { return bar + 8u * (B0 + 4 + x); };
   const uint32_t bDrain = bar + 8u * (B0 + 6);
+  auto bSfree = [&](int x) { return bar + 8u * (B0 + 7 + x); };   // hd 64: softmax X holds S_X in registers
+  auto bPVdone = [&](int x) { return bar + 8u * (B0 + 9 + x); };  // hd 64: P V_X has read P_X, written O_X
+  constexpr bool SPLIT_P = PL::SPLIT_P;
+  static_assert(!SPLIT_P || PL::TM_P + 2 * (BN / 2) <= TMEM_COLS, "TMEM plan");
   uint32_t* misc = reinterpret_cast<uint32_t*>(pk_smem + PL::OFF_MISC);
   volatile uint32_t* abort_flag = misc + 1;
 
@@ -154,6 +165,8 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
       ptx::mbar_init(bSfull(x), 1);
       ptx::mbar_init(bPfull(x), BM);   // every softmax thread of the tile
       ptx::mbar_init(bOfull(x), 1);
+      ptx::mbar_init(bSfree(x), BM);  // every softmax thread of the tile
+      ptx::mbar_init(bPVdone(x), 1);
     }
     ptx::mbar_init(bDrain, 1);
     misc[1] = 0u;
@@ -292,9 +305,12 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
       const bool leader = CONV ? ptx::elect_one() : true;
       // ---------------------------------------------------------- MMA issuer
       // Per segment: S_A(T0), S_B(T0) with K_T0, then per step T the one-shot
-      // order P V_A(T), S_A(T+1), P V_B(T), S_B(T+1).  The first P V of a tile
-      // in a segment overwrites its O; it waits for that tile's first P, which
-      // the softmax writes only after it has read the previous segment's O.
+      // order P V_A(T), S_A(T+1), P V_B(T), S_B(T+1) -- at hd 64, where P has
+      // columns of its own, S_X(T+1) goes first, as soon as softmax X has read
+      // S_X(T).  The first P V of a tile in a segment overwrites its O; it
+      // waits for that tile's first P, which the softmax writes only after it
+      // has read the previous segment's O.  The segment's first S overwrites
+      // S_X: its softmax read the last S before writing the last P.
       constexpr uint32_t IDESC_S = ptx::idesc_f16(BF16, BM, BN, false, false);  // Q, K both K-major
       constexpr uint32_t IDESC_O = ptx::idesc_f16(BF16, BM, HD, false, true);   // P from TMEM, V MN-major
       constexpr uint32_t DHI = ptx::sdesc_sw128_hi(1024);
@@ -311,12 +327,16 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
       };
       auto issue_pv = [&](int x, int slot, bool acc) {
         const uint32_t d = ptx::opaque(tmem + L::TM_O + x * HD);
-        const uint32_t a = ptx::opaque(tmem + L::TM_S + x * BN);  // P_X, 2 elements per column
+        // P_X, 2 elements per column: over S_X (hd 128) or in its own columns (hd 64)
+        const uint32_t a = ptx::opaque(tmem + (SPLIT_P ? PL::TM_P + x * (BN / 2) : L::TM_S + x * BN));
         const uint32_t v = ptx::opaque(ptx::sdesc_sw128_lo(sRing + slot * L::SLOT_BYTES, BN * 128));
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
           if (leader) ptx::mma_f16_ts(d, a + kk * 8, ptx::sdesc_join(v + kk * ((16 * 128) >> 4), DHI), IDESC_O,
                           (acc || kk > 0) ? 1u : 0u);
+        if constexpr (SPLIT_P) {
+          if (leader) ptx::mma_commit(bPVdone(x));
+        }
       };
       int T = 0;               // KV steps issued over the CTA's segments
       int pc0 = 0, pc1 = 0;    // tiles of A / B so far (s_full / p_full phases)
@@ -350,7 +370,16 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
           for (int x = 0; x < 2; ++x) {
             const int nXs = x == 0 ? nAs : nBs;
             if (t < nXs) {
-              ok = mma_wait<CONV>(bPfull(x), ((x == 0 ? pc0 : pc1) + t) & 1, abort_flag, p.watchdog_ns, WD_MMA_P_FULL);
+              const int tile = (x == 0 ? pc0 : pc1) + t;  // tiles of X so far (barrier phases)
+              if constexpr (SPLIT_P) {  // S_X(T+1) as soon as softmax X holds S_X(T) in registers
+                if (t + 1 < nXs) {
+                  ok = mma_wait<CONV>(bSfree(x), tile & 1, abort_flag, p.watchdog_ns, WD_MMA_S_FREE);
+                  if (!ok) break;
+                  ptx::tc_fence_after();
+                  issue_s(x, qset, sk);
+                }
+              }
+              ok = mma_wait<CONV>(bPfull(x), tile & 1, abort_flag, p.watchdog_ns, WD_MMA_P_FULL);
               if (!ok) break;
               ptx::tc_fence_after();
               issue_pv(x, sv, t > 0);
@@ -361,7 +390,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
               else
                 ptx::mma_commit(bEmpty(sv));
             }
-            if (t + 1 < nXs) issue_s(x, qset, sk);
+            if (!SPLIT_P && t + 1 < nXs) issue_s(x, qset, sk);
           }
           if (!ok) break;
           if constexpr (!PAIR_EMPTY) {
@@ -388,6 +417,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + L::TM_S + x * BN;
     const uint32_t tO = tmem + lane_off + L::TM_O + x * HD;
+    const uint32_t tP = SPLIT_P ? tmem + lane_off + PL::TM_P + x * (BN / 2) : tS;  // P_X
     const int off = p.Skv - p.Sq;
     const float sl2 = p.sl2;
     int cnt = 0;   // tiles processed (s_full / p_full phases)
@@ -454,6 +484,10 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
         for (int c = 0; c < BN / 32; ++c) ptx::tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
         ptx::tmem_wait_ld();
         ptx::reg_fence(sr);
+        if constexpr (SPLIT_P) {  // S_X is in registers: the tensor core may compute S_X(T+1) over it
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bSfree(x));
+        }
         float s[BN];
 #pragma unroll
         for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(sr[c]);
@@ -500,7 +534,18 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
           ptx::upk(ptx::add2(ptx::add2(acc[0], acc[1]), ptx::add2(acc[2], acc[3])), a0, a1);
           l += a0 + a1;
         }
-        // the running max moved: rescale O_X in TMEM (P V_X(j-1) finished before S_X(j) did)
+        // the running max moved: rescale O_X in TMEM (hd 128: P V_X(j-1) finished
+        // before S_X(j) did; hd 64: waited for above)
+        if constexpr (SPLIT_P) {
+          // P V_X of the previous tile of this segment has read P_X and written
+          // O_X before this tile touches either (at a segment's first tile the
+          // o_full wait of the previous segment covered it)
+          if (j > jb) {
+            ok = warp_wait_bar(bPVdone(x), (cnt - 1) & 1, abort_flag, p.watchdog_ns, WD_SOFTMAX_PV_DONE);
+            if (!ok) break;
+            ptx::tc_fence_after();
+          }
+        }
         if (j > jb && __any_sync(0xffffffffu, resc)) {
           const uint64_t a2 = ptx::pk(alpha, alpha);
 #pragma unroll
@@ -519,9 +564,9 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
             ptx::tmem_st32(tO + c * 32, orr);
           }
         }
-        // P_X over the first BN/2 columns of S_X
-        ptx::tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pp[0]));
-        ptx::tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pp[32]));
+        // P_X over the first BN/2 columns of S_X (hd 128) or into its own (hd 64)
+        ptx::tmem_st32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pp[0]));
+        ptx::tmem_st32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pp[32]));
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(bPfull(x));

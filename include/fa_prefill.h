@@ -221,12 +221,13 @@ int fa_split_kv_advised(int B, int Hq, int Hkv, int Sq, int Skv, int causal);
  * above it advises split-KV for heads up to 64 wide when there are more
  * query-tile pairs than SMs but the one-shot grid's waves leave SMs idle: the
  * pairs run longest first in waves of one per SM, each wave as long as its
- * longest pair, and when the pairs' KV steps fill less than 88 % of
+ * longest pair, and when the pairs' KV steps fill less than 80 % of
  * SMs x that time, the split-KV schedule's equal stream-K ranges (run by the
  * persistent kernel) finish sooner.  That is the page's split-K rule again --
  * split when the tiles cannot cover the part evenly -- for a grid of a few
- * more pairs than SMs (e.g. the chunked prefill, 256 pairs of ~63 KV steps on
- * 152 SMs).  Host-only; launches nothing.
+ * more pairs than SMs (e.g. 160 equal pairs on 152 SMs fill 53 %; the
+ * chunked prefill's 256 pairs fill 84 % and stay one-shot).  Host-only;
+ * launches nothing.
  */
 int fa_split_kv_advised_hd(int B, int Hq, int Hkv, int Sq, int Skv, int hd, int causal);
 
@@ -386,7 +387,7 @@ unsigned int fa_smem_bytes(int hd);
 /*
  * fa_debug_status -- the kernel watchdog word of the current device: 0 when
  * no kernel has reported a problem since the last clear, otherwise a code
- * (bits 0-7: which wait gave up, 1 to 8 -- or 12, a split piece the schedule
+ * (bits 0-7: which wait gave up, 1 to 11 -- or 12, a split piece the schedule
  * gave no workspace slot (not expected), 17, a persistent kernel whose shared
  * memory was not
  * 1024-byte aligned (nothing run; not expected), 32, a cache-append position

@@ -22,8 +22,8 @@ from causal_prefill_flash_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 
-# producer empty, MMA Q / K-V / P, softmax S / O: the codes of the pipeline waits
-WAIT_CODES = {1, 3, 4, 5, 7, 8}
+# producer empty, MMA Q / K-V / P / S read, softmax S / O / P V done: the codes of the pipeline waits
+WAIT_CODES = {1, 3, 4, 5, 7, 8, 10, 11}
 WD_DRAIN = 9
 TOL = {"f16": 2e-3, "bf16": 8e-3}
 
