@@ -302,6 +302,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                       const __grid_constant__ CUtensorMap tmKt, const __grid_constant__ CUtensorMap tmVt,
                       const Params p) {
+  // heads up to 64 wide run on fa_prefill64_kernel (S and P apart in TMEM)
+  static_assert(HD == 128, "the two-tile kernel with P over S is the 128-column one");
   using L = Layout<HD>;
   constexpr int NSLOT = L::NSLOT;
   // K/V arrive in pairs (V_j, K_j+1) on one barrier, so the MMA thread waits
@@ -470,13 +472,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == MMA_WARP) {
     // ----------------------------------------------------------- MMA issuer
-    // hd 64: the whole warp runs the loop and the waits and one elected lane
-    // issues (its N = 64 P V MMAs make the issuing rate matter: measured +6 %
-    // on the chunked hd 64 prefill); hd 128: lane 0 alone (the converged form
-    // measured -5 to +2 % there)
-    constexpr bool CONV = HD == 64;
-    const bool leader = CONV ? ptx::elect_one() : true;
-    if (CONV || lane == 0) {
+    // lane 0 alone (a converged warp with one elected lane issuing measured
+    // -5 to +2 % here; the hd 64 kernel, where it measured +6 %, uses it)
+    if (lane == 0) {
       constexpr uint32_t IDESC_S = ptx::idesc_f16(BF16, BM, BN, false, false);  // Q, K both K-major
       constexpr uint32_t IDESC_O = ptx::idesc_f16(BF16, BM, HD, false, true);   // P from TMEM, V MN-major
       constexpr uint32_t DHI = ptx::sdesc_sw128_hi(1024);  // Q, K (K-major) and V (MN-major): SBO 1024
@@ -487,9 +485,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t o = ((kk / 4) * (BM * 128) + (kk % 4) * 32) >> 4;
-          if (leader) ptx::mma_f16_ss(d, ptx::sdesc_join(q + o, DHI), ptx::sdesc_join(k + o, DHI), IDESC_S, kk > 0 ? 1u : 0u);
+          ptx::mma_f16_ss(d, ptx::sdesc_join(q + o, DHI), ptx::sdesc_join(k + o, DHI), IDESC_S, kk > 0 ? 1u : 0u);
         }
-        if (leader) ptx::mma_commit(bSfull(x));
+        ptx::mma_commit(bSfull(x));
       };
       auto issue_pv = [&](int x, int slot, bool acc) {
         const uint32_t d = tmem + L::TM_O + x * HD;
@@ -497,34 +495,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t v = ptx::sdesc_sw128_lo(sRing + slot * L::SLOT_BYTES, BN * 128);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          if (leader) ptx::mma_f16_ts(d, a + kk * 8, ptx::sdesc_join(v + kk * ((16 * 128) >> 4), DHI), IDESC_O,
+          ptx::mma_f16_ts(d, a + kk * 8, ptx::sdesc_join(v + kk * ((16 * 128) >> 4), DHI), IDESC_O,
                           (acc || kk > 0) ? 1u : 0u);
       };
-      bool ok = mma_wait<CONV>(bQ, 0, abort_flag, p.watchdog_ns, WD_MMA_Q);  // Q and K_0
+      bool ok = wait_bar(bQ, 0, abort_flag, p.watchdog_ns, WD_MMA_Q);  // Q and K_0
       if (ok && n > 0) {
         ptx::tc_fence_after();
         if (nA > 0) issue_s(0, 0);
         if (nB > 0) issue_s(1, 0);
-        if constexpr (!PAIR_EMPTY) {
-          if (leader) ptx::mma_commit(bEmpty(0));
-        }
+        if constexpr (!PAIR_EMPTY) ptx::mma_commit(bEmpty(0));
       }
       for (int j = 0; ok && j < n; ++j) {
         const int iv = 2 * j + 1, sv = iv % NSLOT;  // V_j
         const int ik = 2 * j + 2, sk = ik % NSLOT;  // K_{j+1}
         const bool more = j + 1 < n;
-        ok = mma_wait<CONV>(bPair(j % NPB), (j / NPB) & 1, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);  // V_j, K_{j+1}
+        ok = wait_bar(bPair(j % NPB), (j / NPB) & 1, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);  // V_j, K_{j+1}
         if (!ok) break;
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
           const int nX = x == 0 ? nA : nB;
           if (j < nX) {
-            ok = mma_wait<CONV>(bPfull(x), j & 1, abort_flag, p.watchdog_ns, WD_MMA_P_FULL);
+            ok = wait_bar(bPfull(x), j & 1, abort_flag, p.watchdog_ns, WD_MMA_P_FULL);
             if (!ok) break;
             ptx::tc_fence_after();
             issue_pv(x, sv, j > 0);
           }
-          if (x == 1 && leader) {
+          if (x == 1) {
             if constexpr (PAIR_EMPTY)
               ptx::mma_commit(bEmpty(j % NPE));  // K_j (its S MMAs came earlier) and V_j, once P V_B(j) is done
             else
@@ -534,13 +530,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (!ok) break;
         if constexpr (!PAIR_EMPTY) {
-          if (more && leader) ptx::mma_commit(bEmpty(sk));
+          if (more) ptx::mma_commit(bEmpty(sk));
         }
       }
-      if (ok && leader) ptx::mma_commit(bOfinal);
+      if (ok) ptx::mma_commit(bOfinal);
       // every MMA issued has finished before TMEM is freed (the softmax may
       // have given up without waiting for o_final)
-      if (leader) ptx::mma_commit(bDrain);
+      ptx::mma_commit(bDrain);
       drain_wait(bDrain, 0, DRAIN_NS);
     }
   }
@@ -1490,7 +1486,9 @@ static int launch(const void* q, const void* k, const void* v, void* o, int hd, 
                   float* lse = nullptr) {
   // heads up to 64 wide run on the kernel with S and P in separate TMEM columns
   constexpr uint32_t REQUEST = HD == 64 ? Layout64::REQUEST : Layout<HD>::REQUEST;
-  auto kern = HD == 64 ? fa_prefill64_kernel<BF16> : fa_prefill_kernel<HD, BF16>;
+  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, Params);
+  if constexpr (HD == 64) kern = fa_prefill64_kernel<BF16>;
+  else kern = fa_prefill_kernel<HD, BF16>;
   const int slot = (HD == 128 ? 2 : 0) + (BF16 ? 1 : 0);
   if (g_attr_set[dev][slot].load() == 0) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)REQUEST) != cudaSuccess) {
