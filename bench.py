@@ -56,8 +56,9 @@ def parse_args(argv=None):
                     help="attention (the default line) or the K/V-cache append of the workload's whole K/V")
     ap.add_argument("--page-size", type=int, default=0,
                     help="read K/V through a paged pool of this page size (a multiple of 128)")
-    ap.add_argument("--path", choices=["auto", "oneshot", "split"], default="auto",
-                    help="kernel: the library's advice for the shape (auto), one-shot, or split-KV")
+    ap.add_argument("--path", choices=["auto", "oneshot", "split", "pair"], default="auto",
+                    help="kernel: the library's advice for the shape (auto), one-shot, split-KV, or the "
+                         "CTA-pair kernel (GQA groups of a multiple of 4, heads 72..128; measurement only)")
     return ap.parse_args(argv)
 
 
@@ -388,6 +389,12 @@ def run_ours(args):
     split = (args.path == "split" or
              (args.path == "auto" and fa.split_kv_advised(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.causal, w.hd)))
     paged = args.page_size > 0
+    pair = args.path == "pair"
+    if pair:
+        if paged or (w.Hq // w.Hkv) % 4 != 0 or not 64 < w.hd <= 128:
+            raise SystemExit("--path pair: the CTA-pair kernel takes contiguous K/V, GQA groups of a multiple "
+                             "of 4 query heads and heads 72..128 wide")
+        fa.debug_force_path("pair")
     if paged:  # each copy's K/V scattered over a pool in shuffled page order
         page = args.page_size
         npg = (w.Skv + page - 1) // page
@@ -543,7 +550,8 @@ def run_ours(args):
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     achieved = flops / (ms_step * 1e-3) / 1e12
-    traffic = recorded_traffic(w.name + (":split" if split else "") + (":paged" if paged else ""))
+    traffic = recorded_traffic(w.name + (":split" if split else "") + (":paged" if paged else "") +
+                               (":pair" if pair else ""))
     line = {
         "metric": "causal prefill attention TFLOPS (ms/call, % of dense peak)",
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -556,7 +564,8 @@ def run_ours(args):
                    "flops_per_call": flops, "flop_convention": "4*hd*visible (query,key) pairs",
                    "l2": f"inputs rotated over {ncopy} resident copies ({ncopy * io / 1e6:.0f} MB > L2)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "kernel": split_kernel_label(fa, w) if split else oneshot_kernel_label(w),
+                   "kernel": split_kernel_label(fa, w) if split else
+                   ("fa_prefill_pair_kernel (CTA pairs, paired MMAs M = 256)" if pair else oneshot_kernel_label(w)),
                    "kv_layout": f"paged, {args.page_size}-token pages in shuffled order" if paged
                    else "contiguous BSHD"},
         "pct_of_peak": 100.0 * achieved / peak,

@@ -97,14 +97,17 @@ def debug_set_watchdog_ns(ns: int) -> None:
     load().fa_debug_set_watchdog_ns(int(ns))
 
 
-PATHS = {"auto": 0, "oneshot": 1, "persistent": 2}
+PATHS = {"auto": 0, "oneshot": 1, "persistent": 2, "pair": 3}
 
 
 def debug_force_path(path: str) -> None:
     """Testing hook: the kernel later calls run on -- "auto" (the library's
-    choice), "oneshot" (the one-shot kernel, also for calls with a workspace)
-    or "persistent" (the persistent kernel: over whole units without a
-    workspace, over every split-KV schedule with one)."""
+    choice), "oneshot" (the one-shot kernel, also for calls with a
+    workspace), "persistent" (the persistent kernel: over whole units without
+    a workspace, over every split-KV schedule with one) or "pair" (the
+    CTA-pair kernel for calls it applies to: GQA groups of a multiple of 4
+    query heads, heads 72 to 128 wide, contiguous K/V; the library's choice
+    for the others)."""
     st = int(load().fa_debug_force_path(PATHS[path]))
     if st != FA_OK:
         raise FaError(st, "fa_debug_force_path")

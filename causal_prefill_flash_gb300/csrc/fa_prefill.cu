@@ -722,6 +722,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 #include "fa_prefill256.cuh"
 #include "fa_prefill64.cuh"
+#include "fa_prefill_pair.cuh"
 
 namespace fa {
 
@@ -1334,17 +1335,17 @@ static EncodeTiledFn encoder() {
   return f;
 }
 
-// 4-D map over a BSHD tensor: dims (hd, H, S, B), box (64, 1, 128, 1), 128-byte swizzle.
+// 4-D map over a BSHD tensor: dims (hd, H, S, B), box (64, 1, box_rows, 1), 128-byte swizzle.
 // A [B][S_stride][H][hd] 16-bit tensor of which rows [0, S) of each batch are
 // described: rows from S on are out of bounds for the map, so TMA loads them
 // as zeros (S_stride = S for a contiguous BSHD tensor; a KV cache's capacity
 // otherwise).
 static bool encode_bshd(CUtensorMap* m, EncodeTiledFn enc, const void* base, bool bf16, int B, int S, int H, int hd,
-                        int S_stride) {
+                        int S_stride, int box_rows = 128) {
   const cuuint64_t rows = (cuuint64_t)(S > 0 ? S : 1), rows_mem = (cuuint64_t)(S_stride > S ? S_stride : rows);
   const cuuint64_t dims[4] = {(cuuint64_t)hd, (cuuint64_t)H, rows, (cuuint64_t)B};
   const cuuint64_t strides[3] = {(cuuint64_t)hd * 2, (cuuint64_t)H * hd * 2, rows_mem * H * hd * 2};
-  const cuuint32_t box[4] = {64, 1, 128, 1};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1380,7 +1381,9 @@ static std::atomic<int> g_pk_attr_set[MAX_DEVICES][4];
 // Kernel selection for testing and measurement (fa_debug_force_path): 0 the
 // library's choice, 1 the one-shot kernel (also for calls with a workspace),
 // 2 the persistent kernel (over whole units without a workspace; for every
-// split-KV schedule with one).
+// split-KV schedule with one), 3 the CTA-pair kernel where it applies (GQA
+// groups of a multiple of 4 query heads, heads 72 to 128 wide, contiguous
+// K/V; measured slower than the single-CTA kernel, so never chosen by default).
 static std::atomic<int> g_force_path{0};
 static std::atomic<int> g_attr256_set[MAX_DEVICES][2];
 
@@ -1404,7 +1407,8 @@ static int check_device(int* dev_out) {
     g_dev_sms[dev].store(sms > 0 ? sms : 1);
     if (major != 10 || minor != 3) st = -FA_ERR_DEVICE;
     else if ((unsigned)optin < Layout<128>::REQUEST || (unsigned)optin < SkLayout<128>::REQUEST ||
-             (unsigned)optin < Layout256::REQUEST || (unsigned)optin < PkLayout<128>::REQUEST)
+             (unsigned)optin < Layout256::REQUEST || (unsigned)optin < PkLayout<128>::REQUEST ||
+             (unsigned)optin < PairLayout::REQUEST)
       st = -FA_ERR_SMEM;
     else st = 1;
     g_dev_ok[dev].store(st);
@@ -1480,10 +1484,71 @@ static bool encode_kv(CUtensorMap* mk, CUtensorMap* mv, CUtensorMap* mkt, CUtens
   return true;
 }
 
+// The CTA-pair kernel (fa_prefill_pair.cuh): heads 72 to 128 wide, contiguous
+// K/V, GQA groups of a multiple of 4 query heads.  Two CTAs per unit of four
+// heads at one 128-row block.  Run only when asked for (fa_debug_force_path(3)):
+// on the 8192-token GQA prefill it measured 504 us per call against 341 us
+// for the single-CTA kernel.
+static std::atomic<int> g_pair_attr_set[MAX_DEVICES][2];
+
+static bool pair_applies(int Hq, int Hkv, const Paged* pg) {
+  return g_force_path.load() == 3 && pg == nullptr && (Hq / Hkv) % 4 == 0;
+}
+
+template <bool BF16>
+static int launch_pair(const void* q, const void* k, const void* v, void* o, int hd, int B, int Hq, int Hkv, int Sq,
+                       int Skv, int kv_cap, int causal, float scale, cudaStream_t stream, int dev, float* lse) {
+  auto kern = fa_prefill_pair_kernel<BF16>;
+  const int slot = BF16 ? 1 : 0;
+  if (g_pair_attr_set[dev][slot].load() == 0) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PairLayout::REQUEST) !=
+        cudaSuccess) {
+      (void)cudaGetLastError();
+      return FA_ERR_SMEM;
+    }
+    g_pair_attr_set[dev][slot].store(1);
+  }
+  EncodeTiledFn enc = encoder();
+  if (!enc) return FA_ERR_LAUNCH;
+  CUtensorMap mq, mkh, mv, mo;
+  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, hd, Sq) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, hd, Sq) ||
+      !encode_bshd(&mkh, enc, k, BF16, B, Skv, Hkv, hd, kv_cap, 64) ||
+      !encode_bshd(&mv, enc, v, BF16, B, Skv, Hkv, hd, kv_cap))
+    return FA_ERR_LAUNCH;
+  Params prm;
+  std::memset(&prm, 0, sizeof(prm));
+  prm.lse = lse;
+  prm.o = static_cast<uint16_t*>(o);
+  prm.hd = hd;
+  prm.B = B;
+  prm.Hq = Hq;
+  prm.Hkv = Hkv;
+  prm.Sq = Sq;
+  prm.Skv = Skv;
+  prm.G = Hq / Hkv;
+  prm.n_qtiles = (Sq + BM - 1) / BM;
+  prm.pair_heads = 1;
+  prm.causal = causal ? 1 : 0;
+  prm.sl2 = scale * 1.4426950408889634f;
+  prm.watchdog_ns = g_watchdog_ns.load();
+  const long long units = (long long)prm.n_qtiles * (Hq / 4) * B;
+  if (2 * units > 0x7FFFFFFFLL) return FA_ERR_UNSUPPORTED;
+  if (launch_pdl(kern, dim3((unsigned)(2 * units)), dim3(NUM_THREADS), PairLayout::REQUEST, stream, mq, mkh, mv, mo,
+                 prm) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return FA_ERR_LAUNCH;
+  }
+  return FA_OK;
+}
+
 template <int HD, bool BF16>
 static int launch(const void* q, const void* k, const void* v, void* o, int hd, int B, int Hq, int Hkv, int Sq, int Skv,
                   int kv_cap, int causal, float scale, cudaStream_t stream, int dev, const Paged* pg = nullptr,
                   float* lse = nullptr) {
+  if constexpr (HD == 128) {
+    if (pair_applies(Hq, Hkv, pg))
+      return launch_pair<BF16>(q, k, v, o, hd, B, Hq, Hkv, Sq, Skv, kv_cap, causal, scale, stream, dev, lse);
+  }
   // heads up to 64 wide run on the kernel with S and P in separate TMEM columns
   constexpr uint32_t REQUEST = HD == 64 ? Layout64::REQUEST : Layout<HD>::REQUEST;
   void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, Params);
@@ -2435,7 +2500,7 @@ extern "C" int fa_debug_status_clear(void) {
 }
 
 extern "C" int fa_debug_force_path(int path) {
-  if (path < 0 || path > 2) return FA_ERR_INVALID_ARG;
+  if (path < 0 || path > 3) return FA_ERR_INVALID_ARG;
   fa::g_force_path.store(path);
   return FA_OK;
 }

@@ -421,7 +421,12 @@ int fa_debug_set_watchdog_ns(unsigned long long ns);
  * default); 1: the one-shot kernel, also for calls given a workspace (no
  * split); 2: the persistent kernel -- over whole query-tile pairs, each CTA
  * taking pairs in snake order, for calls without a workspace, and for every
- * split-KV schedule (not only multi-segment ones) for calls with one.  Heads
+ * split-KV schedule (not only multi-segment ones) for calls with one; 3: the
+ * CTA-pair kernel (two CTAs on two SMs per unit of four query heads, paired
+ * tcgen05 MMAs with M = 256) for the calls it applies to -- contiguous K/V,
+ * GQA groups of a multiple of 4 query heads, heads 72 to 128 wide, no
+ * workspace -- and the library's choice for the others.  (Path 3 measured
+ * slower than the library's choice; it is kept for measurement.)  Heads
  * wider than 128 always run on the one-shot kernel.  The result is the same
  * within the parity tolerance whatever the path.  Host-only.  Returns FA_OK,
  * or FA_ERR_INVALID_ARG for another value (nothing changed).

@@ -23,6 +23,19 @@ def pytest_collection_modifyitems(config, items):
 
 
 @pytest.fixture
+def force_pair():
+    """Run the test's calls on the CTA-pair kernel where it applies (GQA groups
+    of a multiple of 4 query heads, heads 72..128, contiguous K/V); the
+    library's own choice is restored afterwards."""
+    import causal_prefill_flash_gb300 as fa
+    fa.debug_force_path("pair")
+    try:
+        yield
+    finally:
+        fa.debug_force_path("auto")
+
+
+@pytest.fixture
 def force_persistent():
     """Run the test's split-KV calls on the persistent kernel, whatever their
     schedule (the library otherwise runs one-piece-per-CTA schedules on the

@@ -206,3 +206,17 @@ def test_ex_entry_point_errors_without_a_device(fa):
     assert f(*args, 0, 1, 4, 2, 8, 8, 256, 1, 0.1, 0, 6 * A, 1 << 30, 0) == 2     # split-KV: heads up to 128
     assert f(*args, 0, 1, 4, 2, 8, 8, 136, 1, 0.1, 0, 6 * A, 1 << 30, 0) == 2
     assert f(*args, 0, 0, 4, 2, 8, 8, 128, 1, 0.1, 0, 0, 0, 0) == 0               # B = 0
+
+
+def test_force_path_values(fa):
+    """fa_debug_force_path: 0 (library's choice) .. 3 (the CTA-pair kernel);
+    anything else is rejected and leaves the setting alone.  Host-only."""
+    lib = fa._lib.load()
+    try:
+        for path in (0, 1, 2, 3):
+            assert lib.fa_debug_force_path(path) == 0
+        for path in (-1, 4, 1000):
+            assert lib.fa_debug_force_path(path) == 1  # FA_ERR_INVALID_ARG
+        assert set(fa._lib.PATHS.values()) == {0, 1, 2, 3}
+    finally:
+        assert lib.fa_debug_force_path(0) == 0

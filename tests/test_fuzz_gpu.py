@@ -4,9 +4,10 @@ oracle (a GB300 is needed).
 Each case draws B, the GQA grouping, Sq, Skv (Sq may exceed Skv, lengths are
 rarely tile multiples), the head width (a multiple of 8 up to 256), the dtype
 and the mask, then runs the one-shot kernel, the split-KV path as the library
-routes it, and the persistent kernel over whole units and over the split-KV
-schedule (heads up to 128 wide), each into a NaN-prefilled output followed by
-a NaN guard.  Small cases compare every element, larger ones a sample of rows
+routes it, the persistent kernel over whole units and over the split-KV
+schedule (heads up to 128 wide) and, for GQA groups of a multiple of 4 with
+heads 72..128 wide, the CTA-pair kernel, each into a NaN-prefilled output
+followed by a NaN guard.  Small cases compare every element, larger ones a sample of rows
 the oracle computes one by one; the tolerance is the parity tests':
 |o - o_ref| <= tol (1 + |o_ref|), tol = 2e-3 (f16), 8e-3 (bf16).
 """
@@ -47,12 +48,14 @@ def _draw(i):
 CASES = [_draw(i) for i in range(N_CASES)]
 
 
-def _paths(hd):
+def _paths(hd, G):
     yield "oneshot", False, None
     if hd <= 128:
         yield "splitkv", True, None
         yield "persistent", False, "persistent"
         yield "persistent_ws", True, "persistent"
+    if 64 < hd <= 128 and G % 4 == 0:
+        yield "pair", False, "pair"
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "B{}_H{}-{}_Sq{}_Skv{}_hd{}_{}_c{}".format(*c))
@@ -71,7 +74,7 @@ def test_random_shape_every_path(case):
         rows[1] = (B - 1, Hq - 1, Sq - 1)
         want = oracle.attention_rows(q, k, v, rows, causal=causal, scale=w.scale)
     dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
-    for name, split, force in _paths(hd):
+    for name, split, force in _paths(hd, Hq // Hkv):
         buf = torch.full((q.numel() + GUARD,), float("nan"), dtype=q.dtype, device="cuda")
         out = buf[: q.numel()].view(q.shape)
         if force:
