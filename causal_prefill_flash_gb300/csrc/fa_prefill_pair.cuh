@@ -28,8 +28,11 @@
 //   shared memory per CTA: Q_A, Q_B, P_A, P_B (32 KB each), a ring of six
 //     16 KB K/V halves, barriers
 //
-//   warp 9 (both CTAs)   TMA producer: Q_A, Q_B, then the K/V halves
-//   warp 10 (CTA 1)      forwards CTA 1's load completions to CTA 0's barriers
+//   warp 9 (both CTAs)   TMA producer: Q_A, Q_B, then the K/V halves, each
+//                        load counted on its own CTA's barriers (which it
+//                        drains before exit)
+//   warp 11 (both CTAs)  forwards its CTA's load completions to CTA 0's joint
+//                        barriers, which the MMA issuers wait on
 //   warps 8, 10 (CTA 0)  the MMA issuers of tiles A and B for both CTAs, each
 //                        in its tile's own order (S_X(j+1) after s_free,
 //                        P V_X(j) after p_full); their commits arrive on the
@@ -59,7 +62,7 @@ namespace fa {
 
 // Watchdog codes of this kernel (bits 0-7 of g_fa_status), beside the shared ones.
 enum : uint32_t {
-  WD_PAIR_FORWARD = 13,  // CTA 1's forwarder waiting for its own loads
+  WD_PAIR_FORWARD = 13,  // a forwarder waiting for its own CTA's loads
 };
 
 // Register split: the MMA thread builds two operand addresses per MMA (Q or
@@ -79,9 +82,10 @@ struct PairLayout {
   static constexpr uint32_t OFF_P = 2 * Q_BYTES;         // P_A, P_B (and the O staging at the end)
   static constexpr uint32_t OFF_RING = OFF_P + 2 * P_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_RING + NSLOT * HALF_BYTES;
-  // q_full, pair[NPB], empty[NSLOT], s_full[2], s_free[2], p_full[2], pv_done[2],
-  // o_final, drain, o_staged[2]
-  static constexpr uint32_t NUM_BARS = 1 + NPB + NSLOT + 2 + 2 + 2 + 2 + 1 + 1 + 2;
+  // q_full, pair[NPB] (this CTA's own loads), empty[NSLOT], s_full[2], s_free[2],
+  // p_full[2], pv_done[2], o_final, drain, o_staged[2], jq_full, jpair[NPB] (both
+  // CTAs' loads, used in CTA 0)
+  static constexpr uint32_t NUM_BARS = 1 + NPB + NSLOT + 2 + 2 + 2 + 2 + 1 + 1 + 2 + 1 + NPB;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
   static constexpr uint32_t BYTES = OFF_MISC + 16;
   static constexpr uint32_t REQUEST = BYTES + 1024;  // slack to align the dynamic base
@@ -176,6 +180,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   const uint32_t bOfinal = bar + 8u * (B0 + 8);
   const uint32_t bDrain = bar + 8u * (B0 + 9);
   auto bOstaged = [&](int x) { return bar + 8u * (B0 + 10 + x); };
+  const uint32_t bJQ = bar + 8u * (B0 + 12);                        // CTA 0: both CTAs' Q and K_0
+  auto bJPair = [&](int b) { return bar + 8u * (B0 + 13 + b); };  // CTA 0: both CTAs' pair b
   uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + L::OFF_MISC);
   volatile uint32_t* abort_flag = misc + 1;
 
@@ -186,10 +192,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   const int n = kv_tiles(p, w.q0, true);  // KV tiles of the unit (the same for all four heads)
 
   if (threadIdx.x == 0) {
-    // CTA 0's load barriers also count CTA 1's forwarded completions; its
-    // s_free and p_full count one arrival per softmax warp of both CTAs
-    ptx::mbar_init(bQ, rank == 0 ? 2 : 1);
-    for (int b = 0; b < NPB; ++b) ptx::mbar_init(bPair(b), rank == 0 ? 3 : 2);
+    // q_full and pair count this CTA's own loads (its producer drains on
+    // them); CTA 0's jq_full and jpair count one forwarded completion from
+    // each CTA, and its s_free and p_full one arrival per softmax warp of
+    // both CTAs
+    ptx::mbar_init(bQ, 1);
+    for (int b = 0; b < NPB; ++b) {
+      ptx::mbar_init(bPair(b), 2);
+      ptx::mbar_init(bJPair(b), 2);
+    }
+    ptx::mbar_init(bJQ, 2);
     for (int s = 0; s < NSLOT; ++s) ptx::mbar_init(bEmpty(s), 2);  // one commit per MMA issuer
     for (int x = 0; x < 2; ++x) {
       ptx::mbar_init(bSfull(x), 1);
@@ -258,8 +270,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       // a pair whose K was not issued (the last V, or a CTA that gave up):
       // its second arrival without bytes
       if (issued >= 2 && (issued & 1) == 0) ptx::mbar_arrive(bPair(((issued - 2) >> 1) % NPB));
-      // every copy issued has landed before the CTA exits (CTA 0's barriers
-      // also wait for CTA 1's forwarded arrivals, which come unless CTA 1 gave up)
+      // every copy issued has landed before the CTA exits
       drain_wait(bQ, 0, DRAIN_NS);
       const int npairs = issued / 2;  // pairs armed
       for (int b = 0; b < NPB && b < npairs; ++b) {
@@ -267,20 +278,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         drain_wait(bPair(b), (last / NPB) & 1, DRAIN_NS);
       }
     }
-  } else if (warp == PRODUCER_WARP + 1 && rank == 1) {
+  } else if (warp == PRODUCER_WARP + 2) {
     // ----------------------------------------------------------- forwarder
-    // CTA 1's load barriers complete when its own halves have landed; each
-    // completion becomes one arrival on CTA 0's barrier of the same address.
-    // (Pair j + NPB of CTA 1 cannot complete before pair j was forwarded: its
+    // A CTA's own load barriers complete when its halves have landed; each
+    // completion becomes one arrival on CTA 0's joint barrier (a cluster
+    // release from CTA 1: its shared memory is what CTA 0's MMAs read).
+    // (Pair j + NPB of a CTA cannot complete before pair j was forwarded: its
     // loads reuse the slots of pair j, which CTA 0's MMAs free only after
-    // they waited for pair j.)
+    // they waited for the joint pair j.)
     if (lane == 0) {
+      auto forward = [&](uint32_t jb) {
+        if (rank == 0) ptx::mbar_arrive(jb);
+        else ptx::mbar_arrive_cluster(ptx::mapa(jb, 0));
+      };
       // (the Q barrier always: CTA 0 waits for it even when the unit has no KV tile)
       bool ok = wait_bar(bQ, 0, abort_flag, p.watchdog_ns, WD_PAIR_FORWARD);
-      if (ok) ptx::mbar_arrive_cluster(ptx::mapa(bQ, 0));
+      if (ok) forward(bJQ);
       for (int j = 0; ok && j < n; ++j) {
         ok = wait_bar(bPair(j % NPB), (j / NPB) & 1, abort_flag, p.watchdog_ns, WD_PAIR_FORWARD);
-        if (ok) ptx::mbar_arrive_cluster(ptx::mapa(bPair(j % NPB), 0));
+        if (ok) forward(bJPair(j % NPB));
       }
     }
   } else if ((warp == MMA_WARP || warp == PRODUCER_WARP + 1) && rank == 0 && lane == 0) {
@@ -317,7 +333,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       }
       ptx::mma2_commit_both(bPVdone(x));
     };
-    bool ok = wait_bar_cl(bQ, 0, abort_flag, p.watchdog_ns, WD_MMA_Q);  // both CTAs' Q and K_0
+    bool ok = wait_bar_cl(bJQ, 0, abort_flag, p.watchdog_ns, WD_MMA_Q);  // both CTAs' Q and K_0
     if (ok && n > 0) {
       ptx::tc_fence_after();
       issue_s(xi, 0);
@@ -327,7 +343,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const int sv = (2 * j + 1) % NSLOT;  // V_j
       const int sk = (2 * j + 2) % NSLOT;  // K_{j+1}
       const bool more = j + 1 < n;
-      ok = wait_bar_cl(bPair(j % NPB), (j / NPB) & 1, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);  // V_j, K_{j+1}
+      ok = wait_bar_cl(bJPair(j % NPB), (j / NPB) & 1, abort_flag, p.watchdog_ns, WD_MMA_KV_FULL);  // V_j, K_{j+1}
       if (!ok) break;
       if (more) {  // S_X(j+1) as soon as both softmax X hold S_X(j) in registers
         ok = wait_bar_cl(bSfree(xi), j & 1, abort_flag, p.watchdog_ns, WD_MMA_S_FREE);

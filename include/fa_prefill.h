@@ -387,10 +387,10 @@ unsigned int fa_smem_bytes(int hd);
 /*
  * fa_debug_status -- the kernel watchdog word of the current device: 0 when
  * no kernel has reported a problem since the last clear, otherwise a code
- * (bits 0-7: which wait gave up, 1 to 11 -- or 12, a split piece the schedule
- * gave no workspace slot (not expected), 17, a persistent kernel whose shared
- * memory was not
- * 1024-byte aligned (nothing run; not expected), 32, a cache-append position
+ * (bits 0-7: which wait gave up, 1 to 11 or 13 (a CTA pair's load forwarder)
+ * -- or 12, a split piece the schedule gave no workspace slot (not expected),
+ * 17, a persistent kernel whose shared memory was not 1024-byte aligned
+ * (nothing run; not expected), 32, a cache-append position
  * out of range (fa_kv_append), or 33, a block-table entry outside the pool
  * (fa_prefill_paged); bits 8-31: the CTA or token index, saturated).  A
  * pipeline wait that does not complete within the watchdog limit records its

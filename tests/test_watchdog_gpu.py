@@ -22,8 +22,9 @@ from causal_prefill_flash_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 
-# producer empty, MMA Q / K-V / P / S read, softmax S / O / P V done: the codes of the pipeline waits
-WAIT_CODES = {1, 3, 4, 5, 7, 8, 10, 11}
+# producer empty, MMA Q / K-V / P / S read, softmax S / O / P V done, a CTA pair's
+# forwarder: the codes of the pipeline waits
+WAIT_CODES = {1, 3, 4, 5, 7, 8, 10, 11, 13}
 WD_DRAIN = 9
 TOL = {"f16": 2e-3, "bf16": 8e-3}
 
@@ -58,6 +59,7 @@ CASES = [  # (name, B, Hq, Hkv, S, hd, dtype, path)
     ("paged", 2, 8, 4, 1300, 128, "f16", "paged"),
     ("persistent_hd128", 1, 32, 8, 2200, 128, "bf16", "persistent"),
     ("persistent_ws_hd64", 2, 16, 4, 2300, 64, "f16", "persistent_ws"),
+    ("pair_hd128", 1, 16, 4, 1500, 128, "bf16", "pair"),
 ]
 
 
@@ -69,11 +71,11 @@ def test_waits_that_run_out_are_reported_and_leave_the_context_usable(case):
     q, k, v = W.make_inputs(w)
     if path == "paged":
         call = _paged_call(fa, q, k, v, 256, w)
-    elif path.startswith("persistent"):
+    elif path.startswith("persistent") or path == "pair":
         dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
 
         def call(out):
-            fa.debug_force_path("persistent")
+            fa.debug_force_path("pair" if path == "pair" else "persistent")
             try:
                 fa.attention(dq, dk, dv, causal=True, scale=w.scale, out=out, split=path == "persistent_ws")
             finally:
