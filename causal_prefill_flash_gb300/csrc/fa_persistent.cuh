@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
         if constexpr (!PAIR_EMPTY) {
           if (leader) ptx::mma_commit(bEmpty(sk0));
         }
-        if (nseg == 1 && leader) ptx::mma_commit(bQempty(qb));
+        if (NQB == 1 && nseg == 1 && leader) ptx::mma_commit(bQempty(qb));
         for (int t = 0; t < nseg; ++t, ++T) {
           const int sv = (2 * T + 1) % NSLOT;  // V_T
           const int sk = (2 * T + 2) % NSLOT;  // K_T+1
@@ -400,9 +400,14 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
           if constexpr (!PAIR_EMPTY) {
             if (t + 1 < nseg && leader) ptx::mma_commit(bEmpty(sk));
           }
-          if (t + 2 == nseg && leader) ptx::mma_commit(bQempty(qb));  // the segment's last S MMAs are issued
+          if constexpr (NQB == 1) {
+            if (t + 2 == nseg && leader) ptx::mma_commit(bQempty(qb));  // the segment's last S MMAs are issued
+          }
         }
         if (!ok) break;
+        // two Q buffers (hd 64): released with the segment, a commit out of the
+        // step loop (the loop's per-step test cost ~2 % at hd 64)
+        if (NQB > 1 && leader) ptx::mma_commit(bQempty(qb));
         if (nAs > 0 && leader) ptx::mma_commit(bOfull(0));
         if (nBs > 0 && leader) ptx::mma_commit(bOfull(1));
         pc0 += nAs;

@@ -2402,12 +2402,12 @@ static int split_advice(int B, int Hq, int Hkv, int Sq, int Skv, int hd, int cau
   if (2 * units <= sms && longest >= 8) return 1;
   // hd 64: more pairs than SMs, but whole waves of them leave SMs idle --
   // the persistent kernel's stream-K ranges even the load out.  At hd 64 its
-  // whole call (step rate, splits, merge) costs ~1.2x the work of the
-  // one-shot kernel's busy time (chunked prefill: 137.6 us against 135.9 us at
-  // a wave efficiency of 0.835), so it pays below ~0.82; at hd 128 its step is
+  // whole call (step rate, splits, merge) costs ~1.18x the work of the
+  // one-shot kernel's busy time (chunked prefill: 133.1 us against 135.3 us at
+  // a wave efficiency of 0.835), so it pays below ~0.85; at hd 128 its step is
   // 10-15 % slower, more than the quantization it removes
   if (hd != 0 && kernel_hd(hd) == 64 && units > sms && units <= (1 << 20) &&
-      oneshot_wave_efficiency(B, Hq, Hkv, Sq, Skv, causal, static_cast<int>(sms)) < 0.80)
+      oneshot_wave_efficiency(B, Hq, Hkv, Sq, Skv, causal, static_cast<int>(sms)) < 0.85)
     return 1;
   return 0;
 }

@@ -221,13 +221,12 @@ int fa_split_kv_advised(int B, int Hq, int Hkv, int Sq, int Skv, int causal);
  * above it advises split-KV for heads up to 64 wide when there are more
  * query-tile pairs than SMs but the one-shot grid's waves leave SMs idle: the
  * pairs run longest first in waves of one per SM, each wave as long as its
- * longest pair, and when the pairs' KV steps fill less than 80 % of
+ * longest pair, and when the pairs' KV steps fill less than 85 % of
  * SMs x that time, the split-KV schedule's equal stream-K ranges (run by the
  * persistent kernel) finish sooner.  That is the page's split-K rule again --
- * split when the tiles cannot cover the part evenly -- for a grid of a few
- * more pairs than SMs (e.g. 160 equal pairs on 152 SMs fill 53 %; the
- * chunked prefill's 256 pairs fill 84 % and stay one-shot).  Host-only;
- * launches nothing.
+ * split when the tiles cannot cover the part evenly -- for a grid of more
+ * pairs than SMs (e.g. 160 equal pairs on 152 SMs fill 53 %; the chunked
+ * prefill's 256 pairs fill 84 %).  Host-only; launches nothing.
  */
 int fa_split_kv_advised_hd(int B, int Hq, int Hkv, int Sq, int Skv, int hd, int causal);
 

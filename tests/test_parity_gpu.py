@@ -286,9 +286,9 @@ def test_workload_full_size_sampled_rows(idx, split):
 def test_split_advice_follows_the_grid_fill():
     """The library advises split-KV where the one-shot grid leaves most SMs
     idle and rows are long (the long-context chunk), and -- knowing the head
-    width -- for hd 64 grids of a few more pairs than SMs whose waves leave
-    many SMs idle (160 equal pairs on 152 SMs); not for the workloads below,
-    not at hd 128 or 256."""
+    width -- for hd 64 grids of more pairs than SMs whose waves leave many SMs
+    idle (160 equal pairs on 152 SMs; the chunked hd 64 prefill's 256 pairs);
+    not for the workloads below, not at hd 128 or 256."""
     fa = _fa()
     W_ = {w.name: w for w in W.WORKLOADS}
     adv = lambda w: fa.split_kv_advised(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.causal)
@@ -298,7 +298,8 @@ def test_split_advice_follows_the_grid_fill():
                  "chunked_kv8192_hd128", "chunked_kv8192_hd64", "encoder_s4096_noncausal",
                  "gqa_s4096_hd256_bf16"):
         assert not adv(W_[name]), name
-        assert not adv_hd(W_[name]), name
+        assert adv_hd(W_[name]) == (name == "chunked_kv8192_hd64" and
+                                   torch.cuda.get_device_properties(0).multi_processor_count == 152), name
     # 10 sequences x 16 head pairs of one 128-row tile over 8192 keys: 160 equal
     # pairs, two waves on 152 SMs, the second almost empty
     sms = torch.cuda.get_device_properties(0).multi_processor_count
