@@ -55,7 +55,6 @@ def simulate(nslot, npb, n, seed, plant=None):
     fwd_busy = [0.0, 0.0]
     # CTA 0's joint barriers
     joint_q = [0]  # arrivals (completes at 2)
-    joint_pair_arrivals = [[0] * 0 for _ in range(npb)]
     joint_pair_done = [0] * npb
     joint_pair_open = [0] * npb  # arrivals in the open phase
     joint_q_done = [False]
