@@ -1,4 +1,4 @@
-"""Tensors past 2^31 elements (a GB300 is needed).
+"""Tensors past 2^31 elements, and grid extremes (a GB300 is needed).
 
 B = 1, Hq = 64, Hkv = 8, Sq = Skv = 262144, hd = 128, bf16, causal: Q and O
 hold exactly 2^31 elements each (4 GiB), so the rows at the end of the
@@ -64,3 +64,26 @@ def test_outputs_beyond_32_bit_offsets(split):
         want_lse = oracle.lse_rows(q1, k1, np.array([[0, 0, 0]]), causal=True, scale=scale)[0]
         got_lse = float(lse[0, hq, i].item())
         assert abs(got_lse - want_lse) <= 2e-4 * (1 + abs(want_lse)), (hq, i, got_lse, want_lse)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Skv,hd,dtype", [
+    (2048, 2, 1, 7, 7, 128, "f16"),       # thousands of sequences of a few tokens
+    (1, 128, 1, 300, 300, 128, "bf16"),   # one KV head for 128 query heads
+    (1, 256, 256, 129, 129, 64, "f16"),   # many heads, one row past a tile
+    (3, 96, 32, 200, 3000, 8, "bf16"),    # the narrowest heads, GQA 3, chunked
+])
+def test_extreme_shapes(B, Hq, Hkv, Sq, Skv, hd, dtype):
+    """Grid extremes against the oracle on every element (inputs from the
+    seeded workload generator), through the library's own path choice."""
+    from causal_prefill_flash_gb300 import workloads as W
+    fa = _fa()
+    w = W.Workload("extreme", B, Hq, Hkv, Sq, Skv, hd, causal=True, dtype=dtype, seed=B + Hq + Sq)
+    q, k, v = W.make_inputs(w)
+    out = fa.attention(q.cuda(), k.cuda(), v.cuda(), causal=True, scale=w.scale)
+    torch.cuda.synchronize()
+    assert fa.debug_status() == 0
+    want = oracle.attention(q, k, v, causal=True, scale=w.scale)
+    got = out.cpu().double().numpy()
+    tol = 2e-3 if dtype == "f16" else 8e-3
+    err = np.abs(got - want)
+    assert (err <= tol * (1 + np.abs(want))).all(), f"max err {err.max():.3e}"
