@@ -48,11 +48,12 @@
 // global memory is touched only after griddepcontrol.wait.
 //
 // The same translation unit holds the other kernels of the library, which
-// share these helpers: the split-KV kernel for one piece per CTA
-// (fa_prefill_sk_kernel, below) and its merge, the persistent kernel that
-// runs split-KV schedules with several segments per CTA
-// (fa_persistent.cuh), the hd = 256 kernel (fa_prefill256.cuh) and the
-// K/V-cache append (kv_append.cuh).
+// share these helpers: the hd <= 64 kernel with S and P in separate TMEM
+// columns (fa_prefill64.cuh), the hd = 256 kernel (fa_prefill256.cuh), the
+// split-KV kernel for one piece per CTA (fa_prefill_sk_kernel, below) and its
+// merge, the persistent kernel that runs split-KV schedules with several
+// segments per CTA (fa_persistent.cuh), the opt-in kernel on CTA pairs
+// (fa_prefill_pair.cuh) and the K/V-cache append (kv_append.cuh).
 
 #include <cuda.h>
 #include <cuda_bf16.h>
