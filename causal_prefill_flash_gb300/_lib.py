@@ -49,6 +49,7 @@ _SIG = {
     "fa_debug_set_watchdog_ns": (_I, [ctypes.c_ulonglong]),
     "fa_debug_force_path": (_I, [ctypes.c_int]),
     "fa_debug_schedule": (_I, [_I] * 7 + [_P, _P, _P, _I, _P]),
+    "fa_debug_row_pairing": (_I, [_I] * 7),
 }
 
 
@@ -131,6 +132,16 @@ def debug_schedule(B, Hq, Hkv, Sq, Skv, causal=True, sms=152):
     G = out[0]
     return {"pairs": nu, "ctas": G, "one_segment": bool(out[1]), "split_pairs": out[2], "slots": out[3],
             "cta_pair": list(cp[: G + 1]), "cta_step": list(cs[: G + 1]), "pair_steps": list(ps[:nu])}
+
+
+def debug_row_pairing(B, Hq, Hkv, Sq, Skv, causal=True, sms=152) -> bool:
+    """Whether the one-shot grid leaves query tile 0 without a partner (True)
+    or the last tile (False, also when no tile goes alone) for a shape on a
+    GPU of ``sms`` SMs (host-only)."""
+    st = int(load().fa_debug_row_pairing(int(B), int(Hq), int(Hkv), int(Sq), int(Skv), int(bool(causal)), int(sms)))
+    if st < 0:
+        raise FaError(-st, "fa_debug_row_pairing")
+    return bool(st)
 
 
 def _ptr(x) -> int:

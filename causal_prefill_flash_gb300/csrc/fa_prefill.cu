@@ -64,7 +64,9 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <functional>
 #include <mutex>
+#include <queue>
 #include <utility>
 #include <vector>
 
@@ -138,7 +140,8 @@ struct Params {
   int B, Hq, Hkv, Sq, Skv;
   int G;           // Hq / Hkv
   int n_qtiles;    // ceil(Sq / BM)
-  int pair_heads;  // 1: tiles A, B = query heads 2p, 2p+1 at the same rows; 0: rows 2t, 2t+1 of one head
+  int pair_heads;  // 1: tiles A, B = query heads 2p, 2p+1 at the same rows; 0: two adjacent row tiles of one head
+  int lone_first;  // row tiles, odd tile count: 1 = tile 0 without a partner, 0 = the last tile (pair_first_tile)
   int causal;
   float sl2;       // scale * log2(e)
   unsigned long long watchdog_ns;
@@ -166,6 +169,22 @@ struct Work {
   bool has[2];
 };
 
+// First query tile of row pair pq (MHA and odd GQA groups: one head, two
+// adjacent 128-row tiles per CTA).  An even tile count pairs (2 pq, 2 pq + 1).
+// An odd one leaves one tile without a partner: the last (pairs (2 pq,
+// 2 pq + 1), tile B missing at the last pq) or, with lone_first, tile 0
+// (tile 0 alone at pq = 0, then (2 pq - 1, 2 pq)).  Under the causal mask the
+// last tile sees the most keys and tile 0 the fewest; the host picks the
+// pairing whose grid it expects to finish first (lone_tile_first).
+__host__ __device__ __forceinline__ int pair_first_tile(int n_qtiles, int lone_first, int pq) {
+  if (!(n_qtiles & 1) || !lone_first) return 2 * pq;
+  return pq == 0 ? 0 : 2 * pq - 1;
+}
+__host__ __device__ __forceinline__ bool pair_has_b(int n_qtiles, int lone_first, int pq) {
+  if (!(n_qtiles & 1)) return true;
+  return lone_first ? pq > 0 : 2 * pq + 1 < n_qtiles;
+}
+
 __device__ __forceinline__ Work decode_work(const Params& p) {
   Work w;
   if (p.pair_heads) {
@@ -186,10 +205,10 @@ __device__ __forceinline__ Work decode_work(const Params& p) {
     const int rem = static_cast<int>(blockIdx.x % per);
     w.b = rem / p.Hq;
     w.hq[0] = w.hq[1] = rem % p.Hq;
-    w.q0[0] = 2 * pq * BM;
+    w.q0[0] = pair_first_tile(p.n_qtiles, p.lone_first, pq) * BM;
     w.q0[1] = w.q0[0] + BM;
     w.has[0] = true;
-    w.has[1] = w.q0[1] < p.Sq;
+    w.has[1] = pair_has_b(p.n_qtiles, p.lone_first, pq);
   }
   w.hk = w.hq[0] / p.G;
   return w;
@@ -821,9 +840,9 @@ __host__ __device__ __forceinline__ UnitGeo unit_geo(const Params& p, int u) {
     const int rem = u % per;
     w.b = rem / p.Hq;
     w.hq0 = w.hq1 = rem % p.Hq;
-    w.q00 = 2 * pq * BM;
+    w.q00 = pair_first_tile(p.n_qtiles, p.lone_first, pq) * BM;
     w.q01 = w.q00 + BM;
-    w.has1 = w.q01 < p.Sq;
+    w.has1 = pair_has_b(p.n_qtiles, p.lone_first, pq);
   }
   w.hk = w.hq0 / p.G;
   w.nA = geo_kv_tiles(p, w.q00);
@@ -1368,6 +1387,53 @@ static long long unit_count_of(const Params& p) {
   return ((n_qt + 1) / 2) * (long long)p.Hq * p.B;
 }
 
+// Row-pair grids with an odd tile count: which tile goes without a partner
+// (pair_first_tile).  A list-scheduling model of the one-shot grid (CTAs in
+// launch order, each to the SM that frees first) decides: a CTA costs its KV
+// steps -- 0.65 of a step each when it holds one tile, whose chain leaves the
+// tensor core idle much of the time -- plus 2.5 steps of fixed cost.  Tile 0
+// alone cuts the grid's total steps, which counts from ~1.5 waves on (2432
+// and 2659-token MHA prefills measured +6 % and +3 %, 24 heads of GQA 3
+// +5.5 %); near one wave the longest CTA sets the time, and a pair there is
+// slower than the last tile alone (1152 tokens: -8 %), as the model has it.
+// Cached per shape.
+static int lone_tile_first(const Params& prm0, int sms) {
+  if (prm0.pair_heads || !(prm0.n_qtiles & 1) || prm0.n_qtiles < 3 || sms < 1) return 0;
+  const long long nu = unit_count_of(prm0);
+  if (nu > (1 << 16)) return 1;  // many waves: the total decides
+  static std::mutex mu;
+  static int cache[8][8];
+  static int n_cached = 0, next = 0;
+  const int key[7] = {prm0.B, prm0.Hq, prm0.Hkv, prm0.Sq, prm0.Skv, prm0.causal, sms};
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < n_cached; ++i)
+      if (std::memcmp(cache[i], key, sizeof(key)) == 0) return cache[i][7];
+  }
+  double span[2];
+  for (int lf = 0; lf < 2; ++lf) {
+    Params prm = prm0;
+    prm.lone_first = lf;
+    std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+    for (int i = 0; i < sms; ++i) free_at.push(0.0);
+    span[lf] = 0.0;
+    for (long long u = 0; u < nu; ++u) {
+      const UnitGeo w = unit_geo(prm, static_cast<int>(u));
+      const double t = free_at.top() + (w.has1 ? w.n : 0.65 * w.n) + 2.5;
+      free_at.pop();
+      free_at.push(t);
+      span[lf] = std::max(span[lf], t);
+    }
+  }
+  const int lf = span[1] < 0.99 * span[0] ? 1 : 0;
+  std::lock_guard<std::mutex> lk(mu);
+  std::memcpy(cache[next], key, sizeof(key));
+  cache[next][7] = lf;
+  next = (next + 1) % 8;
+  if (n_cached < 8) ++n_cached;
+  return lf;
+}
+
 constexpr int MAX_DEVICES = 64;
 
 // The wait limit the next launches give their kernels (fa_debug_set_watchdog_ns).
@@ -1582,6 +1648,7 @@ static int launch(const void* q, const void* k, const void* v, void* o, int hd, 
   prm.n_qtiles = (Sq + BM - 1) / BM;
   prm.pair_heads = (prm.G % 2 == 0) ? 1 : 0;
   prm.causal = causal ? 1 : 0;
+  prm.lone_first = lone_tile_first(prm, g_dev_sms[dev].load());
   prm.sl2 = scale * 1.4426950408889634f;
   prm.watchdog_ns = g_watchdog_ns.load();
   const long long grid = grid_size(B, Hq, Hkv, Sq);
@@ -1918,6 +1985,7 @@ static int launch_sk(const void* q, const void* k, const void* v, void* o, int h
   prm.n_qtiles = (Sq + BM - 1) / BM;
   prm.pair_heads = (prm.G % 2 == 0) ? 1 : 0;
   prm.causal = causal ? 1 : 0;
+  prm.lone_first = 1;  // split-KV: fewer steps in total
   prm.sl2 = scale * 1.4426950408889634f;
   prm.block_table = pkv.block_table;
   prm.page_size = pkv.page_size;
@@ -1979,6 +2047,7 @@ static int launch_pk(const void* q, const void* k, const void* v, void* o, int h
   prm.n_qtiles = (Sq + BM - 1) / BM;
   prm.pair_heads = (prm.G % 2 == 0) ? 1 : 0;
   prm.causal = causal ? 1 : 0;
+  prm.lone_first = ws_o ? 1 : lone_tile_first(prm, g_dev_sms[dev].load());  // split-KV: fewer steps in total
   prm.sl2 = scale * 1.4426950408889634f;
   prm.block_table = pkv.block_table;
   prm.page_size = pkv.page_size;
@@ -2245,6 +2314,7 @@ static int launch_sk_static(const void* q, const void* k, const void* v, void* o
   prm.n_qtiles = (Sq + BM - 1) / BM;
   prm.pair_heads = (prm.G % 2 == 0) ? 1 : 0;
   prm.causal = causal ? 1 : 0;
+  prm.lone_first = 1;  // split-KV: fewer steps in total
   prm.sl2 = scale * 1.4426950408889634f;
   prm.watchdog_ns = g_watchdog_ns.load();
   SkSchedule sc;
@@ -2377,6 +2447,7 @@ static double oneshot_wave_efficiency(int B, int Hq, int Hkv, int Sq, int Skv, i
   prm.n_qtiles = (Sq + BM - 1) / BM;
   prm.pair_heads = (prm.G % 2 == 0) ? 1 : 0;
   prm.causal = causal ? 1 : 0;
+  prm.lone_first = lone_tile_first(prm, sms);  // the one-shot grid's pairing
   const long long nu = unit_count_of(prm);
   long long total = 0, makespan = 0;
   for (long long u = 0; u < nu; ++u) {
@@ -2457,6 +2528,7 @@ extern "C" int fa_debug_schedule(int B, int Hq, int Hkv, int Sq, int Skv, int ca
   prm.n_qtiles = (Sq + fa::BM - 1) / fa::BM;
   prm.pair_heads = (prm.G % 2 == 0) ? 1 : 0;
   prm.causal = causal ? 1 : 0;
+  prm.lone_first = 1;  // as the split-KV path
   const long long nu = fa::unit_count_of(prm);
   if (nu > 0x7FFFFFFF) return -FA_ERR_UNSUPPORTED;
   if (pair_steps && nu > max_pairs) return -FA_ERR_UNSUPPORTED;
@@ -2473,6 +2545,22 @@ extern "C" int fa_debug_schedule(int B, int Hq, int Hkv, int Sq, int Skv, int ca
   out[2] = sc.n_split;
   out[3] = sc.slots;
   return static_cast<int>(nu);
+}
+
+extern "C" int fa_debug_row_pairing(int B, int Hq, int Hkv, int Sq, int Skv, int causal, int sms) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Sq < 1 || Skv < 1 || sms < 1) return -FA_ERR_INVALID_ARG;
+  fa::Params prm;
+  std::memset(&prm, 0, sizeof(prm));
+  prm.B = B;
+  prm.Hq = Hq;
+  prm.Hkv = Hkv;
+  prm.Sq = Sq;
+  prm.Skv = Skv;
+  prm.G = Hq / Hkv;
+  prm.n_qtiles = (Sq + fa::BM - 1) / fa::BM;
+  prm.pair_heads = (prm.G % 2 == 0) ? 1 : 0;
+  prm.causal = causal ? 1 : 0;
+  return fa::lone_tile_first(prm, sms);
 }
 
 extern "C" unsigned int fa_smem_bytes(int hd) {

@@ -80,6 +80,7 @@
  *   fa_debug_set_watchdog_ns         testing hook: the kernels' wait limit
  *   fa_debug_force_path              testing hook: which kernel runs
  *   fa_debug_schedule                the split-KV work split for a shape
+ *   fa_debug_row_pairing             the one-shot grid's pairing of query tiles
  */
 #ifndef FA_PREFILL_H
 #define FA_PREFILL_H
@@ -453,6 +454,24 @@ int fa_debug_force_path(int path);
 int fa_debug_schedule(int B, int Hq, int Hkv, int Sq, int Skv, int causal, int sms,
                       int* cta_pair, int* cta_step, int* pair_steps, int max_pairs,
                       int* out);
+
+/*
+ * fa_debug_row_pairing -- which query tile of a head the one-shot grid leaves
+ * without a partner, for a shape on a GPU of `sms` SMs (host-only, no device
+ * call; for tests and tools).  It matters for row pairs (MHA or an odd GQA
+ * group: a CTA holds two adjacent 128-row tiles of one head) with an odd tile
+ * count.  Under the causal mask tile 0 sees the fewest keys and the last tile
+ * the most; a CTA's time follows its KV steps, and one tile alone walks them
+ * little faster than a pair.  So leaving tile 0 alone cuts the grid's total
+ * steps, while near one wave the longest CTA sets the time and the last tile
+ * alone is shorter than a pair there.  The library takes the pairing that a
+ * list-scheduling model of the grid expects to finish first; the split-KV
+ * paths always leave tile 0 alone (their ranges even out the lengths).
+ * Returns 1 when tile 0 goes alone (then pairs (2p - 1, 2p)), 0 when the last
+ * tile does (pairs (2p, 2p + 1)) or no tile goes alone (head pairs, even tile
+ * counts, one tile), -FA_ERR_INVALID_ARG for a bad shape or sms < 1.
+ */
+int fa_debug_row_pairing(int B, int Hq, int Hkv, int Sq, int Skv, int causal, int sms);
 
 #ifdef __cplusplus
 }

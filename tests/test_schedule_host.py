@@ -153,3 +153,43 @@ def test_static_scratch_bound_holds_for_every_schedule(fa):
         worst = max(worst, need)
         assert need <= 40 * 1024 * 1024
     assert worst <= 40763392
+
+
+def test_row_pairing_choice(fa):
+    """Which tile of a head the one-shot grid leaves without a partner (odd
+    tile counts of row pairs): the last one near one wave of CTAs, where the
+    longest CTA sets the time, and tile 0 from ~1.5 waves on, where the total
+    of the CTAs' KV steps does; nothing when no tile goes alone."""
+    assert not fa.debug_row_pairing(1, 32, 32, 2048, 2048, True, SMS)  # even tile count
+    assert not fa.debug_row_pairing(1, 32, 8, 2659, 2659, True, SMS)   # head pairs (GQA 4)
+    assert not fa.debug_row_pairing(1, 4, 4, 100, 100, True, SMS)      # one tile
+    assert not fa.debug_row_pairing(1, 32, 32, 1152, 1152, True, SMS)  # 160 CTAs
+    assert fa.debug_row_pairing(1, 40, 40, 1152, 1152, True, SMS)      # 200 CTAs
+    assert fa.debug_row_pairing(1, 32, 32, 2659, 2659, True, SMS)      # 352 CTAs
+    assert fa.debug_row_pairing(1, 24, 8, 2659, 2659, True, SMS)       # GQA 3, 264 CTAs
+    assert not fa.debug_row_pairing(1, 40, 40, 1152, 1152, False, SMS)  # equal CTAs: no gain
+    with pytest.raises(fa.FaError):
+        fa.debug_row_pairing(1, 3, 2, 100, 100, True, SMS)
+
+
+def _kv_tiles(Sq, Skv, causal, t):
+    off = Skv - Sq
+    q_last = min(128 * t + 128, Sq) - 1
+    hi = min(Skv, off + q_last + 1) if causal else Skv
+    return -(-hi // 128) if hi > 0 else 0
+
+
+@pytest.mark.parametrize("shape", [(1, 4, 4, 1152, 1152, True), (1, 3, 1, 2659, 2659, True),
+                                   (2, 2, 2, 300, 700, True), (1, 2, 2, 1152, 1152, False)])
+def test_split_pairs_leave_tile_0_alone(fa, shape):
+    """The split-KV paths pair the tiles of an odd count as (0), (1, 2),
+    (3, 4), ...: the pairs' KV steps, longest first with the heads inner,
+    follow from that pairing alone."""
+    B, Hq, Hkv, Sq, Skv, causal = shape
+    n_qt = -(-Sq // 128)
+    assert n_qt % 2 == 1
+    want = []
+    for pq in range((n_qt + 1) // 2 - 1, -1, -1):
+        tiles = [0] if pq == 0 else [2 * pq - 1, 2 * pq]
+        want += [max(_kv_tiles(Sq, Skv, causal, t) for t in tiles)] * (B * Hq)
+    assert fa.debug_schedule(B, Hq, Hkv, Sq, Skv, causal, sms=SMS)["pair_steps"] == want
