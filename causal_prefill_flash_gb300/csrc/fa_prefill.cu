@@ -121,8 +121,8 @@ struct Layout {
   static constexpr uint32_t OFF_RING = 2 * Q_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_RING + NSLOT * SLOT_BYTES;
   // q_full (Q and K_0), pair[NPB <= NSLOT] (V_j, K_j+1), empty[NSLOT] (hd 128: pair-empty, NPE of them),
-  // s_full[2], p_full[2], o_final, drain, o_staged[2]
-  static constexpr uint32_t NUM_BARS = 1 + 2 * NSLOT + 2 + 2 + 2 + 2;
+  // s_full[2], p_full[2], o_final, drain
+  static constexpr uint32_t NUM_BARS = 1 + 2 * NSLOT + 2 + 2 + 2;
   // [0] TMEM base, [1] abort flag, [2], [3] barrier and phase of tile A's early o_final (0: none)
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr uint32_t BYTES = OFF_MISC + 16;
@@ -357,7 +357,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto bPfull = [&](int x) { return bar + 8u * (3 + 2 * NSLOT + x); };
   const uint32_t bOfinal = bar + 8u * (5 + 2 * NSLOT);
   const uint32_t bDrain = bar + 8u * (6 + 2 * NSLOT);
-  auto bOstaged = [&](int x) { return bar + 8u * (7 + 2 * NSLOT + x); };  // O tile x written to its ring slot
   uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + L::OFF_MISC);
   volatile uint32_t* abort_flag = misc + 1;
 
@@ -379,8 +378,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     ptx::mbar_init(bOfinal, 1);
     ptx::mbar_init(bDrain, 1);
-    ptx::mbar_init(bOstaged(0), 4);  // one arrival per softmax warp of the tile
-    ptx::mbar_init(bOstaged(1), 4);
     misc[1] = 0u;
     // tile A's early o_final (row pairs, hd 128): the slot-free barrier of step nA-1
     uint32_t early_bar = 0u, early_par = 0u;
@@ -684,8 +681,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (ok && hasx) {
       if (p.lse && q0 + r < p.Sq) p.lse[(static_cast<size_t>(w.b) * p.Hq + hqx) * p.Sq + q0 + r] = row_lse(m_ref, l);
       // O / l rounded to 16 bits, written 128-byte swizzled (the layout of a Q
-      // tile) and sent out by TMA tensor stores, one per 64-column block: the
-      // global writes are whole lines, and rows past Sq are clipped by the map.
+      // tile) and sent out by TMA tensor stores, one per warp and 64-column
+      // block: the global writes are whole lines, and rows past Sq are
+      // clipped by the map.
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
       // Stage slots: tile A in the slot of load 2n-4 (K_n-2), tile B in that
       // of load 2n-3 (V_n-2).  When tile A's O is final, only loads from
@@ -714,16 +712,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       ptx::fence_proxy_async_smem();  // make the generic-proxy writes visible to the TMA unit
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bOstaged(x));
-      if ((warp & 3) == 0) {
-        ok = warp_wait_bar(bOstaged(x), 0, abort_flag, p.watchdog_ns, WD_SOFTMAX_O_DONE);
-        if (ok && lane == 0) {
+      // each warp sends its own 32 rows (the map's box is 64 columns x 32
+      // rows), so no warp waits for the tile's other three
+      const int r0 = 32 * (warp & 3);
+      if (lane == 0 && q0 + r0 < p.Sq) {
 #pragma unroll
-          for (int c = 0; c < (int)L::KCH; ++c)
-            ptx::tma_store_4d(&tmO, sRing + stage_slot * L::SLOT_BYTES + c * (BM * 128), c * 64, hqx, q0, w.b);
-          ptx::bulk_commit();
-          ptx::bulk_wait_read0();  // the slot must stay valid until the TMA unit has read it
-        }
+        for (int c = 0; c < (int)L::KCH; ++c)
+          ptx::tma_store_4d(&tmO, sRing + stage_slot * L::SLOT_BYTES + c * (BM * 128) + r0 * 128, c * 64, hqx,
+                            q0 + r0, w.b);
+        ptx::bulk_commit();
+        ptx::bulk_wait_read0();  // the slot must stay valid until the TMA unit has read it
       }
     }
   }
@@ -1633,7 +1631,9 @@ static int launch(const void* q, const void* k, const void* v, void* o, int hd, 
   if (!enc) return FA_ERR_LAUNCH;
   CUtensorMap mq, mk, mv, mo, mkt, mvt;
   Params prm;
-  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, hd, Sq) || !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, hd, Sq) ||
+  // the 128-wide kernel stores O per warp, 32 rows a box
+  if (!encode_bshd(&mq, enc, q, BF16, B, Sq, Hq, hd, Sq) ||
+      !encode_bshd(&mo, enc, o, BF16, B, Sq, Hq, hd, Sq, HD == 128 ? 32 : 128) ||
       !encode_kv(&mk, &mv, &mkt, &mvt, enc, k, v, BF16, B, Skv, kv_cap, Hkv, hd, pg, &prm))
     return FA_ERR_LAUNCH;
   prm.lse = lse;

@@ -49,10 +49,11 @@ def test_smem_request_matches_the_tile_layout(fa):
     """Two query tiles + a ring of K/V slots (5 at hd = 128, 8 at hd = 64) +
     the mbarriers + 16 B of flags + 1 KB alignment slack; within the 227 KB
     opt-in limit.  hd 128: one for Q, a full/empty pair per slot, two each
-    for S ready and P ready, the final O, the abort drain, two O-staged.
-    hd 64: one for Q, 4 (V, K) pair barriers, 8 slot frees, two each for S
-    ready, S read, P ready and P V done, the final O, the drain, two O-staged."""
-    for hd, nslot, bars in ((64, 8, 1 + 4 + 8 + 2 * 4 + 1 + 1 + 2), (128, 5, 1 + 2 * 5 + 2 + 2 + 2 + 2)):
+    for S ready and P ready, the final O and the abort drain (each warp sends
+    its own rows of O, so no O-staged barrier).  hd 64: one for Q, 4 (V, K)
+    pair barriers, 8 slot frees, two each for S ready, S read, P ready and
+    P V done, the final O, the drain, two O-staged."""
+    for hd, nslot, bars in ((64, 8, 1 + 4 + 8 + 2 * 4 + 1 + 1 + 2), (128, 5, 1 + 2 * 5 + 2 + 2 + 2)):
         q = 128 * hd * 2
         slot = 128 * hd * 2
         want = 2 * q + nslot * slot + bars * 8 + 16 + 1024
