@@ -193,3 +193,13 @@ def test_split_pairs_leave_tile_0_alone(fa, shape):
         tiles = [0] if pq == 0 else [2 * pq - 1, 2 * pq]
         want += [max(_kv_tiles(Sq, Skv, causal, t) for t in tiles)] * (B * Hq)
     assert fa.debug_schedule(B, Hq, Hkv, Sq, Skv, causal, sms=SMS)["pair_steps"] == want
+
+
+def test_row_pairing_cache_is_consistent(fa):
+    """The choice is cached per shape (eight entries): more shapes than
+    entries, asked twice in a different order, give the same answers."""
+    shapes = [(1, h, h, s, s, True) for h in (24, 32, 40) for s in (1152, 1400, 2432, 2659)]
+    first = {sh: fa.debug_row_pairing(*sh, SMS) for sh in shapes}
+    again = {sh: fa.debug_row_pairing(*sh, SMS) for sh in reversed(shapes)}
+    assert first == again
+    assert any(first.values()) and not all(first.values())
