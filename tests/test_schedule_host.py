@@ -23,6 +23,8 @@ SHAPES = [  # (B, Hq, Hkv, Sq, Skv, causal)
     (1, 32, 32, 2048, 2048, True),    # 256 pairs: stream-K ranges
     (1, 32, 8, 8192, 8192, True),     # 1024 pairs
     (4, 32, 8, 512, 8192, True),      # chunked prefill, 256 pairs
+    (1, 32, 32, 2659, 2659, True),    # odd tile count (tile 0 alone), 352 pairs: stream-K ranges
+    (1, 24, 8, 1152, 3000, True),     # GQA 3, odd tile count, keys ahead of the queries
 ]
 
 
